@@ -1,0 +1,22 @@
+"""CPU oracle (float64, numpy) for the joint video-audio sCM + DMD objective.
+
+TEST INFRASTRUCTURE ONLY: imported by the test suite, the smoke check and the
+benchmark's CPU-baseline leg. The CUDA library never uses it.
+"""
+
+from .t2va_oracle import (  # noqa: F401
+    decode,
+    dmd_objective,
+    dmd_residual_scale,
+    encode,
+    joint_jvp,
+    l2_normalise,
+    noise,
+    round_to_bf16_bits,
+    scm_direction,
+    scm_objective,
+    stage3_objective,
+    trigflow_field,
+    trigflow_noise,
+    valid_samples,
+)
