@@ -1,0 +1,553 @@
+"""Benchmark of the joint video-audio distillation objective on B300.
+
+One step = one pass of the whole hot path over one batch of synthetic inputs:
+TrigFlow noising of (z0, eps) and of (zhat0, eps'), then the fused stage-3
+sCM + DMD objective (forward + gradient), all through the C ABI. The default
+workload is the 512x768 stage-3 shape (B=4, video [128,16,16,24], audio
+[126,128], bf16 inputs, float32 gradients).
+
+Prints one JSON line. `value` is the whole-job throughput in GB/s of algorithmic
+HBM bytes (each input read once, each output written once) with inputs resident
+in device memory; `roofline` describes the dominant kernel (the fused objective),
+timed live with CUDA events recorded inside the captured graph; `e2e` is the
+same metric with host buffers (pinned host -> device copies of the inputs and
+device -> host copies of the gradients and losses inside the timed region);
+`cpu_baseline` is the float64 CPU oracle timed on a bounded sample.
+
+`--impl reference` times the CPU oracle itself as the reference arm.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic as S  # noqa: E402
+
+METRIC = "fused joint sCM+DMD objective GB/s (fwd+grad) and % of B300 HBM peak"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = "stage3_512x768_bf16"
+FALLBACK_HBM_GBS = 6400.0
+OBJECTIVE_SOURCES = ["joint_video_audio_02_b300/csrc/t2va_objective.cu",
+                     "joint_video_audio_02_b300/csrc/t2va_internal.cuh"]
+TRAFFIC_FILE = "profiles/stage3_objective_512x768_traffic.txt"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+
+def elem_size(dtype: str) -> int:
+    return {"bf16": 2, "f32": 4}[dtype]
+
+
+def bytes_per_element(call: str, dtype: str) -> int:
+    """Each input read once, each output written once; gradients are float32."""
+    e = elem_size(dtype)
+    return {"noise": 3 * e, "scm": 4 * e + 4, "dmd": 3 * e + 4, "stage3": 7 * e + 2 * 4}[call]
+
+
+def step_bytes(wl: S.Workload) -> dict:
+    n = wl.batch * sum(wl.numels)
+    out = {"elements": n}
+    if wl.mode == S.STAGE3:
+        out["noise"] = 2 * n * bytes_per_element("noise", wl.dtype)
+        out["objective"] = n * bytes_per_element("stage3", wl.dtype)
+    elif wl.mode == S.SCM:
+        out["noise"] = n * bytes_per_element("noise", wl.dtype)
+        out["objective"] = n * bytes_per_element("scm", wl.dtype)
+    else:
+        out["noise"] = 0
+        out["objective"] = n * bytes_per_element("dmd", wl.dtype)
+    out["step"] = out["noise"] + out["objective"]
+    return out
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def objective_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in OBJECTIVE_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """DRAM bytes per launch of the objective kernel from the committed ncu summary,
+    if it was taken on the current kernel source and this workload; else None."""
+    try:
+        kv = {}
+        with open(os.path.join(ROOT, TRAFFIC_FILE)) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256") != objective_source_hash() or kv.get("workload") != workload:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    REASONS = {
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
+    }
+
+    def __init__(self, index: int, period_s: float = 0.005):
+        self.samples = []
+        self.period = period_s
+        self.stop_evt = threading.Event()
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            self.max_mhz = None
+        self.thread = threading.Thread(target=self._run, daemon=True)
+
+    def _run(self):
+        while not self.stop_evt.is_set():
+            try:
+                mhz = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
+                rs = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append((time.perf_counter(), mhz, rs))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self.thread.start()
+
+    def stop(self):
+        self.stop_evt.set()
+        if self.ok:
+            self.thread.join()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml_unavailable"], "samples": 0}
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside and self.samples:
+            mid = 0.5 * (t0 + t1)
+            inside = [min(self.samples, key=lambda s: abs(s[0] - mid))]
+        mhz = [s[1] for s in inside]
+        bits = 0
+        for s in inside:
+            bits |= s[2]
+        reasons = sorted({name for b, name in self.REASONS.items() if bits & b and b != 0x1})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
+    import torch
+
+    import joint_video_audio_02_b300 as t2va
+    from joint_video_audio_02_b300.build import build
+
+    build()
+    t2va.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    nb = step_bytes(wl)
+    M = wl.num_modalities
+    dt = wl.dtype
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+
+    # rotating input sets: together at least 3x the L2 size, so no step finds its inputs in L2
+    set_bytes = nb["step"] + 2 * wl.batch * sum(wl.numels) * elem_size(dt)
+    R = max(2, math.ceil(3 * l2 / set_bytes))
+    fields_in = ["z0", "eps", "x0_teacher", "x0_student", "x0_tangent"]
+    if wl.mode == S.STAGE3:
+        fields_in += ["zhat0", "eps_hat", "x0_teacher_hat", "x0_fake"]
+
+    def to_dev(a):
+        if dt == "bf16":
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    sets = []
+    host0 = None
+    for r in range(R):
+        inp = S.make_workload_inputs(wl, seed_offset=1000 * rank + r)
+        if r == 0:
+            host0 = inp
+        d = {f: [to_dev(a) for a in getattr(inp, f)] for f in fields_in}
+        d["t"] = torch.from_numpy(inp.t).to(dev)
+        d["zt"] = [torch.empty_like(x) for x in d["z0"]]
+        d["gS"] = [torch.empty(x.shape, dtype=torch.float32, device=dev) for x in d["z0"]]
+        if wl.mode == S.STAGE3:
+            d["zht"] = [torch.empty_like(x) for x in d["zhat0"]]
+            d["gD"] = [torch.empty(x.shape, dtype=torch.float32, device=dev) for x in d["z0"]]
+        d["loss"] = torch.empty(wl.batch, device=dev)
+        d["norm"] = torch.empty(wl.batch * M, device=dev)
+        d["cdmd"] = torch.empty(wl.batch * M, device=dev)
+        sets.append(d)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = t2va.new_workspace(wl.batch, M)
+    torch.cuda.synchronize()
+
+    def objective(d, stream=None):
+        if wl.mode == S.STAGE3:
+            t2va.stage3_objective(d["zt"], d["x0_teacher"], d["x0_student"], d["x0_tangent"], d["t"],
+                                  d["zhat0"], d["x0_teacher_hat"], d["x0_fake"], beta=wl.beta,
+                                  gamma=wl.gamma, eps_scm=wl.eps_scm, eps_dmd=wl.eps_dmd,
+                                  weight=wl.weight, lambda_scm=wl.lambda_scm, lambda_dmd=wl.lambda_dmd,
+                                  grad_x0_student=d["gS"], grad_zhat0=d["gD"], loss=d["loss"],
+                                  norm=d["norm"], cdmd=d["cdmd"], workspace=ws, status=status,
+                                  stream=stream)
+        else:
+            t2va.scm_objective(d["zt"], d["x0_teacher"], d["x0_student"], d["x0_tangent"], d["t"],
+                               beta=wl.beta, gamma=wl.gamma, eps_scm=wl.eps_scm, weight=wl.weight,
+                               lambda_scm=wl.lambda_scm, grad_x0_student=d["gS"], loss=d["loss"],
+                               norm=d["norm"], workspace=ws, status=status, stream=stream)
+
+    def noise(d, stream=None):
+        t2va.noise(d["z0"], d["eps"], d["zt"], d["t"], status=status, stream=stream)
+        if wl.mode == S.STAGE3:
+            t2va.noise(d["zhat0"], d["eps_hat"], d["zht"], d["t"], status=status, stream=stream)
+
+    launches_per_step = (2 if wl.mode == S.STAGE3 else 1) + 1
+
+    # capture: graph of S steps with external timing events around each objective launch
+    K, W = args.steps, args.warmup
+    S_steps = min(K, 1000)
+    cap_stream = torch.cuda.Stream(device=dev)
+    cap_stream.wait_stream(torch.cuda.current_stream())
+    ev_s = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(S_steps)]
+    ev_e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(S_steps)]
+
+    def capture(nsteps, with_events, offset=0):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap_stream):
+            with torch.cuda.graph(g, stream=cap_stream):
+                for i in range(nsteps):
+                    d = sets[(offset + i) % R]
+                    noise(d, cap_stream)
+                    if with_events:
+                        ev_s[i].record(cap_stream)
+                    objective(d, cap_stream)
+                    if with_events:
+                        ev_e[i].record(cap_stream)
+        return g
+
+    # eager warm-up of every set once (also first-call attribute setup), then capture
+    with torch.cuda.stream(cap_stream):
+        for d in sets:
+            noise(d, cap_stream)
+            objective(d, cap_stream)
+    cap_stream.synchronize()
+    g_main = capture(S_steps, True)
+    reps, rem = divmod(K, S_steps)
+    g_rem = capture(rem, False, offset=S_steps) if rem else None
+    g_warm = capture(W, False) if W > 0 else None
+    torch.cuda.synchronize()
+
+    # warm-up steps
+    with torch.cuda.stream(cap_stream):
+        if g_warm is not None:
+            g_warm.replay()
+    cap_stream.synchronize()
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.05)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    h0 = time.perf_counter()
+    with torch.cuda.stream(cap_stream):
+        t_start.record(cap_stream)
+        for _ in range(reps):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        t_end.record(cap_stream)
+    cap_stream.synchronize()
+    torch.cuda.synchronize()
+    h1 = time.perf_counter()
+    if dist is not None:
+        dist.barrier()
+    time.sleep(0.02)
+    sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    obj_ms = [ev_s[i].elapsed_time(ev_e[i]) for i in range(S_steps)]
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st} during the benchmark")
+
+    if dist is not None:
+        import torch.distributed as tdist
+        tt = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+
+    ms_per_step = elapsed_ms / K
+    value = world * nb["step"] * K / (elapsed_ms * 1e-3) / 1e9
+    obj_mean_ms = float(np.mean(obj_ms))
+    obj_gbs = nb["objective"] / (obj_mean_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    clocks = sampler.summary(h0, h1)
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, wl, host0, sets[0], ws, status, noise, objective, dev, nb, world, dist)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dt, "data": "synthetic",
+        "config": {"workload": wl.name, "global_batch": wl.batch * world, "per_gpu_batch": wl.batch,
+                   "latent_shapes": [list(s) for s in wl.shapes], "mode": wl.mode,
+                   "elements_per_step": nb["elements"] * world,
+                   "algorithmic_bytes_per_step": nb["step"] * world,
+                   "parallelism": f"replicas x{world} (samples sharded by rank, no collective)",
+                   "l2": f"rotating {R} input sets ({R * set_bytes / 2**20:.0f} MiB >= 3x L2 "
+                         f"{l2 / 2**20:.0f} MiB): no step finds its inputs in L2",
+                   "timing": "CUDA graph replay; CUDA events on the launching stream"},
+        "elements_per_s": nb["elements"] * world * K / (elapsed_ms * 1e-3),
+        "hbm_fraction_of_step": round(value / world / peak, 4),
+        "roofline": {"kernel": "t2va stage-3 objective" if wl.mode == S.STAGE3 else "t2va sCM objective",
+                     "bound": "hbm", "achieved": round(obj_gbs, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(obj_gbs / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6400 GB/s",
+                     "traffic": committed_traffic(wl.name),
+                     "algorithmic_bytes_per_launch": nb["objective"],
+                     "mean_launch_us": round(obj_mean_ms * 1e3, 3),
+                     "launches_timed": S_steps,
+                     "frac_of_nominal_8TBps": round(obj_gbs / 8000.0, 4)},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+    }
+    return result
+
+
+def run_e2e(args, wl, host0, d0, ws, status, noise, objective, dev, nb, world, dist):
+    """Same step with pinned host inputs copied in and gradients/losses copied out."""
+    import torch
+
+    steps = max(3, min(args.steps, args.e2e_steps))
+    fields = ["z0", "eps", "x0_teacher", "x0_student", "x0_tangent", "t"]
+    if wl.mode == S.STAGE3:
+        fields += ["zhat0", "eps_hat", "x0_teacher_hat", "x0_fake"]
+    pinned = {}
+    h2d = 0
+    for f in fields:
+        if f == "t":
+            ts = [torch.from_numpy(host0.t).pin_memory()]
+        else:
+            arrs = getattr(host0, f)
+            if wl.dtype == "bf16":
+                ts = [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for a in arrs]
+            else:
+                ts = [torch.from_numpy(a).pin_memory() for a in arrs]
+        pinned[f] = ts
+        h2d += sum(x.numel() * x.element_size() for x in ts)
+    outs = ["gS", "loss"] + (["gD"] if wl.mode == S.STAGE3 else [])
+    host_out = {k: [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (d0[k] if isinstance(d0[k], list) else [d0[k]])]
+                for k in outs}
+    d2h = sum(x.numel() * x.element_size() for v in host_out.values() for x in v)
+    stream = torch.cuda.Stream(device=dev)
+
+    def one():
+        with torch.cuda.stream(stream):
+            for f in fields:
+                dst = [d0["t"]] if f == "t" else d0[f]
+                for a, b in zip(dst, pinned[f]):
+                    a.copy_(b, non_blocking=True)
+            noise(d0, stream)
+            objective(d0, stream)
+            for k in outs:
+                src = d0[k] if isinstance(d0[k], list) else [d0[k]]
+                for a, b in zip(host_out[k], src):
+                    a.copy_(b, non_blocking=True)
+
+    one()
+    stream.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1)
+    if dist is not None:
+        import torch.distributed as tdist
+        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        ms = float(tt.item())
+    assert int(status.item()) == 0
+    return {"value": round(world * nb["step"] * steps / (ms * 1e-3) / 1e9, 3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": ms / steps}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_pass(wl: S.Workload, inp: S.Inputs):
+    import oracle
+    dt = wl.dtype
+    zt = oracle.noise(inp.z0, inp.eps, inp.t, dt)
+    if wl.mode == S.STAGE3:
+        oracle.noise(inp.zhat0, inp.eps_hat, inp.t, dt)
+        oracle.stage3_objective(zt, inp.x0_teacher, inp.x0_student, inp.x0_tangent, inp.t,
+                                inp.zhat0, inp.x0_teacher_hat, inp.x0_fake, wl.beta, wl.gamma,
+                                wl.eps_scm, wl.eps_dmd, wl.weight, wl.lambda_scm, wl.lambda_dmd, dt)
+    else:
+        oracle.scm_objective(zt, inp.x0_teacher, inp.x0_student, inp.x0_tangent, inp.t, wl.beta,
+                             wl.gamma, wl.eps_scm, wl.weight, wl.lambda_scm, dt)
+
+
+def bounded_sample(wl: S.Workload, frac: float) -> S.Workload:
+    """The workload cut to one sample whose latents keep `frac` of each modality's elements."""
+    import dataclasses
+    numels = [max(16, int(n * frac)) for n in wl.numels]
+    return dataclasses.replace(wl, batch=1, shapes=tuple((n,) for n in numels), t_fixed=None)
+
+
+def cpu_baseline(wl: S.Workload, budget_s: float) -> dict:
+    """The oracle, as it stands, on sample 0 of the workload, repeated for about budget_s."""
+    one = bounded_sample(wl, 1.0)
+    inp = S.make_workload_inputs(one)
+    nbytes = step_bytes(one)["step"]
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_pass(one, inp)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes * reps / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"sample 0 of {wl.batch} ({sum(one.numels):,} elements: noising + objective), "
+                      f"{reps} passes in {dt:.1f} s; numpy float64, single thread"}
+
+
+def run_reference(args, wl: S.Workload, world: int):
+    """The oracle as the reference arm: each step a bounded sample of the workload."""
+    probe = bounded_sample(wl, 0.05)
+    pinp = S.make_workload_inputs(probe)
+    t0 = time.perf_counter()
+    oracle_pass(probe, pinp)
+    rate = sum(probe.numels) / max(time.perf_counter() - t0, 1e-6)   # elements / s
+    budget = min(120.0, max(20.0, 3.0 * (args.steps + args.warmup)))
+    per_step = budget / max(1, args.steps + args.warmup)
+    frac = min(1.0, per_step * rate / sum(wl.numels))
+    one = bounded_sample(wl, frac)
+    inp = S.make_workload_inputs(one)
+    for _ in range(args.warmup):
+        oracle_pass(one, inp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_pass(one, inp)
+    dt = time.perf_counter() - t0
+    nbytes = step_bytes(one)["step"]
+    value = nbytes * args.steps / dt / 1e9
+    sample = (f"per step: one sample holding {frac:.4f} of each latent of the workload "
+              f"({sum(one.numels):,} elements), noising + objective")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "global_batch": wl.batch, "per_gpu_batch": wl.batch,
+                       "latent_shapes": [list(s) for s in wl.shapes], "mode": wl.mode,
+                       "reference": "float64 CPU oracle (numpy), the parity reference of this library"},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(S.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 0 or args.steps < 1:
+        ap.error("--steps >= 1 and --warmup >= 0")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = S.workload(args.workload)
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, wl, world)), flush=True)
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        tdist.init_process_group("nccl", rank=rank, world_size=world,
+                                  device_id=torch.device("cuda", local))
+        dist = tdist
+    result = run_gpu(args, wl, rank, world, dist)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(wl, args.cpu_baseline_seconds)
+        else:
+            result["cpu_baseline"] = None
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * t2va.h - C ABI of the joint video-audio distillation objective library
+ * (TurboT2VA joint sCM + DMD objective; NVIDIA B300, sm_103a).
+ *
+ * The library computes, on the GPU, one data-parallel step of TurboT2VA's
+ * distillation objective over paired video and audio latents that share one
+ * timestep per sample: TrigFlow noising, the joint sCM direction with its
+ * per-sample, per-modality L2 normalisation, the DMD term with its
+ * residual-scale normaliser, the per-sample losses and the float32 gradients
+ * with respect to the student outputs.
+ *
+ * Sources (cited per entry point below):
+ *   [zh] "TurboT2VA：分数正则化一致性蒸馏加速 19B 视频音频联合生成，四步采样
+ *        20.1×、H20 上全栈 54.67×" (robotworld.top/zh/papers/paper-2608.24674),
+ *        sections 三, 3.1, 四, 4.1 (the only page printing the equations).
+ *   [en] "TurboT2VA: Score-Regularized Consistency Distillation for Fast
+ *        Large-Scale Text-to-Video-Audio Generation"
+ *        (robotworld.top/en/papers/paper-2608.24674): Eq. 6 (per-modality L2
+ *        normalisation), Eq. 11-12 (DMD residual-scale normaliser).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - A batch holds `batch` samples; each sample has `num_modalities` latents
+ *   (modality 0 = video, 1 = audio in the paper; up to T2VA_MAX_MODALITIES).
+ * - Latent m of sample b is seg[m].numel contiguous elements starting at
+ *   element b * seg[m].sample_stride of each per-modality buffer. All buffers of
+ *   one modality (inputs and float32 gradients) share this geometry; the
+ *   element order inside a sample is irrelevant (the objective reduces over all
+ *   elements of a sample and modality).
+ * - Pointer arrays (`const void* const* x`) are HOST arrays of num_modalities
+ *   DEVICE pointers. Every device pointer must be 16-byte aligned. Scalars `t`
+ *   (per-sample timesteps, float32 [batch]) and the outputs are DEVICE pointers.
+ *   `weight` is a HOST array of num_modalities floats (w_m).
+ * - Inputs are float32 or bfloat16 (`dtype`); arithmetic is float32 with
+ *   float32 accumulation; gradients are written in float32.
+ * - The caller owns every buffer and the stream. The library allocates no
+ *   device memory, keeps no state across calls except inside the caller's
+ *   workspace, and never synchronises the host: calls are asynchronous on
+ *   `stream`. Outputs must not overlap inputs.
+ * - Return value: T2VA_SUCCESS or a synchronous error code (argument checks,
+ *   launch failure); nothing is enqueued when an error is returned. Problems
+ *   found on the device set bits in the caller's device int `*status`
+ *   (OR-ed, never cleared by the library).
+ * - Tails and per-sample offsets that are not multiples of the 16-byte vector
+ *   width are handled, not rejected.
+ */
+#ifndef T2VA_H
+#define T2VA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define T2VA_ABI_VERSION 1
+#define T2VA_MAX_MODALITIES 4
+
+typedef enum t2va_dtype {
+  T2VA_FLOAT32 = 0,
+  T2VA_BFLOAT16 = 1
+} t2va_dtype;
+
+/* Geometry of one modality: elements per sample and the distance (in elements)
+ * between the first elements of consecutive samples (>= numel when batch > 1). */
+typedef struct t2va_segment {
+  int64_t numel;
+  int64_t sample_stride;
+} t2va_segment;
+
+/* Synchronous return codes. */
+enum {
+  T2VA_SUCCESS = 0,
+  T2VA_ERROR_INVALID_ARGUMENT = 1,  /* bad size, scalar or null pointer          */
+  T2VA_ERROR_UNSUPPORTED_DTYPE = 2, /* dtype is not T2VA_FLOAT32/T2VA_BFLOAT16     */
+  T2VA_ERROR_MISALIGNED = 3,        /* a device pointer is not 16-byte aligned     */
+  T2VA_ERROR_WORKSPACE = 4,         /* workspace null, misaligned or too small     */
+  T2VA_ERROR_CUDA = 5               /* a CUDA runtime call or launch failed        */
+};
+
+/* Device status bits, OR-ed into *status by the kernels. */
+#define T2VA_STATUS_BAD_TIMESTEP 0x1  /* a sample's t is outside (0, pi/2): its outputs are NaN    */
+#define T2VA_STATUS_TIMEOUT 0x2       /* a cross-CTA wait ran out; outputs of the call are invalid
+                                         and the workspace must be re-initialised                 */
+#define T2VA_STATUS_BAD_WORKSPACE 0x4 /* the workspace was not initialised (or is poisoned by a
+                                         timeout); nothing was computed                          */
+
+/* Static description of a return code (never NULL). */
+const char* t2va_error_string(int code);
+
+/* T2VA_ABI_VERSION of the loaded library. */
+int t2va_abi_version(void);
+
+/* Bytes of workspace needed by the objective entry points for up to `batch`
+ * samples of `num_modalities` modalities on the CURRENT device (the size
+ * depends on its SM count). Returns 0 on invalid arguments or if no device
+ * can be queried. */
+size_t t2va_workspace_bytes(int batch, int num_modalities);
+
+/* Prepare a workspace (16-byte aligned device memory of `workspace_bytes`)
+ * for use on `stream`: clears the cross-CTA counters and records the wait
+ * limit `timeout_ms` (0 selects 1000 ms) after which a kernel gives up and
+ * sets T2VA_STATUS_TIMEOUT instead of waiting on. Must be called once before
+ * the first objective call that uses this workspace, and again after a
+ * TIMEOUT. Calls that may run concurrently need distinct workspaces. */
+int t2va_workspace_init(void* workspace, size_t workspace_bytes, uint32_t timeout_ms,
+                        cudaStream_t stream);
+
+/* TrigFlow noising  ([zh] section 三, the noising equation; [en] section 2):
+ *   z_t^m = cos(t_b) * z0^m + sin(t_b) * eps^m    for every modality m,
+ * with one shared t_b per sample and independent eps per modality. z0, eps and
+ * zt have the same dtype; zt may be the same buffer as z0 or eps (in place).
+ * Results are rounded to the output dtype (round to nearest even); every finite
+ * t is accepted. `status` may be NULL; a non-finite t sets
+ * T2VA_STATUS_BAD_TIMESTEP. Reads 2 and writes 1 element per latent element. */
+int t2va_noise(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+               const void* const* z0, const void* const* eps, void* const* zt,
+               const float* t, int* status, cudaStream_t stream);
+
+/* Joint sCM objective  ([zh] 3.1; [en] Eq. 6). Per sample b and modality m,
+ * with c = cos t_b, s = sin t_b and elementwise
+ *   F_T = (c z_t - x0_teacher)/s,  F_theta = (c z_t - x0_student)/s,
+ *   J   = c s (dF_theta/dt + dF_theta/dz^v F_T^v + dF_theta/dz^a F_T^a)
+ *         assembled from `x0_student_tangent`, the tangent of the student x0
+ *         prediction along (dt, dz^v, dz^a) = (1, F_T^v, F_T^a),
+ *   g   = -beta c / sqrt(1 - gamma^2 s^2) (sg(F_theta) - F_T) - gamma c s z_t - J,
+ *   g_bar = g / (||g||_2 + eps_scm)    (norm over the sample's elements of m),
+ *   r   = F_theta - sg(F_theta) - g_bar,
+ * it writes
+ *   loss[b] = lambda_scm * sum_m weight[m] ||r_m||^2          (device float [batch]),
+ *   norm[b*M + m] = ||g_m||_2      (device float [batch*M], may be NULL),
+ *   grad_x0_student[m] = d(sum_b loss[b]) / d x0_student = 2 lambda w_m g_bar / s
+ *     (float32, same geometry as the inputs; added to the buffer's contents
+ *      when `accumulate` is non-zero, overwritten otherwise).
+ * The whole g_bar is a stop-gradient target. Requires beta finite,
+ * 0 <= gamma <= 1, eps_scm > 0, weight[m] >= 0. A sample with t outside
+ * (0, pi/2) gets NaN outputs and sets T2VA_STATUS_BAD_TIMESTEP. `workspace`
+ * must be initialised by t2va_workspace_init and hold
+ * t2va_workspace_bytes(batch, M) bytes. `status` is required. */
+int t2va_scm_objective(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+                       const void* const* z_t, const void* const* x0_teacher,
+                       const void* const* x0_student, const void* const* x0_student_tangent,
+                       const float* t, float beta, float gamma, float eps_scm,
+                       const float* weight, float lambda_scm,
+                       float* const* grad_x0_student, int accumulate,
+                       float* loss, float* norm,
+                       void* workspace, size_t workspace_bytes, int* status,
+                       cudaStream_t stream);
+
+/* Joint DMD objective  ([zh] 四; [en] Eq. 11-12). On the re-noised on-policy
+ * sample, with y_T = x0_teacher_hat and y_fake = x0_fake (the teacher and
+ * fake-score x0 predictions at zhat_t):
+ *   g = y_fake - y_T,  c_m = (1/N_m) sum_i |zhat0_i - y_T,i|,
+ *   g_bar = g / (c_m + eps_dmd),  Delta = zhat0 - sg(zhat0 - g_bar),
+ *   loss[b] = lambda_dmd * sum_m weight[m] sum_i Delta_i^2   (a sum over elements),
+ *   cdmd[b*M + m] = c_m  (may be NULL),
+ *   grad_zhat0[m] = 2 lambda_dmd w_m g_bar (float32; `accumulate` as above).
+ * A modality with numel 0 contributes 0 and reports c_m = 0. Requires
+ * eps_dmd > 0, weight[m] >= 0. Does not depend on t. */
+int t2va_dmd_objective(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+                       const void* const* zhat0, const void* const* x0_teacher_hat,
+                       const void* const* x0_fake, float eps_dmd, const float* weight,
+                       float lambda_dmd, float* const* grad_zhat0, int accumulate,
+                       float* loss, float* cdmd,
+                       void* workspace, size_t workspace_bytes, int* status,
+                       cudaStream_t stream);
+
+/* Stage-3 objective  ([zh] 4.1; [en] section 3):
+ *   loss[b] = lambda_scm L_sCM,b + lambda_dmd L_DMD,b
+ * over the same batch and the same per-sample t, with both terms as defined
+ * above and one set of weights w_m. Reads the seven inputs once and writes both
+ * gradients once, in one launch. `loss_scm` and `loss_dmd` (device float
+ * [batch], each already multiplied by its lambda) may be NULL, as may `norm`
+ * and `cdmd`. If grad_zhat0[m] == grad_x0_student[m] (the caller's on-policy
+ * sample is the student output itself), the two gradients are summed into
+ * that one buffer. A sample with t outside (0, pi/2) gets NaN in every output. */
+int t2va_stage3_objective(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+                          const void* const* z_t, const void* const* x0_teacher,
+                          const void* const* x0_student, const void* const* x0_student_tangent,
+                          const float* t,
+                          const void* const* zhat0, const void* const* x0_teacher_hat,
+                          const void* const* x0_fake,
+                          float beta, float gamma, float eps_scm, float eps_dmd,
+                          const float* weight, float lambda_scm, float lambda_dmd,
+                          float* const* grad_x0_student, float* const* grad_zhat0, int accumulate,
+                          float* loss, float* loss_scm, float* loss_dmd, float* norm, float* cdmd,
+                          void* workspace, size_t workspace_bytes, int* status,
+                          cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* T2VA_H */

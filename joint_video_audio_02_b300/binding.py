@@ -1,0 +1,234 @@
+"""Thin ctypes binding of the C ABI in include/t2va.h.
+
+Argument marshalling only: every tensor is a CUDA tensor owned by the caller,
+every step of the computation runs in libt2va.so's kernels on the caller's
+current (or given) stream. There is no CPU path; loading fails loudly if the
+library is not built.
+
+A latent of modality m is a tensor whose first dimension is the sample and
+whose remaining dimensions are contiguous; all tensors of one modality share
+that geometry (the gradients too, in float32).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence
+
+import torch
+
+from .build import LIB
+
+c_int, c_float, c_void_p, c_size_t, c_int64, c_uint32 = (
+    ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int64, ctypes.c_uint32)
+
+T2VA_FLOAT32 = 0
+T2VA_BFLOAT16 = 1
+MAX_MODALITIES = 4
+
+STATUS_BAD_TIMESTEP = 0x1
+STATUS_TIMEOUT = 0x2
+STATUS_BAD_WORKSPACE = 0x4
+
+EXPORTED = ("t2va_error_string", "t2va_abi_version", "t2va_workspace_bytes", "t2va_workspace_init",
+            "t2va_noise", "t2va_scm_objective", "t2va_dmd_objective", "t2va_stage3_objective")
+
+
+class Segment(ctypes.Structure):
+    _fields_ = [("numel", c_int64), ("sample_stride", c_int64)]
+
+
+class T2VAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: t2va error {code}: {error_string(code)}")
+
+
+_LIB = None
+
+
+def _declare(lib):
+    P = c_void_p
+    lib.t2va_error_string.argtypes = [c_int]
+    lib.t2va_error_string.restype = ctypes.c_char_p
+    lib.t2va_abi_version.argtypes = []
+    lib.t2va_abi_version.restype = c_int
+    lib.t2va_workspace_bytes.argtypes = [c_int, c_int]
+    lib.t2va_workspace_bytes.restype = c_size_t
+    lib.t2va_workspace_init.argtypes = [P, c_size_t, c_uint32, P]
+    lib.t2va_workspace_init.restype = c_int
+    seg = ctypes.POINTER(Segment)
+    lib.t2va_noise.argtypes = [c_int, c_int, seg, c_int, P, P, P, P, P, P]
+    lib.t2va_noise.restype = c_int
+    lib.t2va_scm_objective.argtypes = [c_int, c_int, seg, c_int, P, P, P, P, P,
+                                       c_float, c_float, c_float, P, c_float,
+                                       P, c_int, P, P, P, c_size_t, P, P]
+    lib.t2va_scm_objective.restype = c_int
+    lib.t2va_dmd_objective.argtypes = [c_int, c_int, seg, c_int, P, P, P, c_float, P, c_float,
+                                       P, c_int, P, P, P, c_size_t, P, P]
+    lib.t2va_dmd_objective.restype = c_int
+    lib.t2va_stage3_objective.argtypes = [c_int, c_int, seg, c_int, P, P, P, P, P, P, P, P,
+                                          c_float, c_float, c_float, c_float, P, c_float, c_float,
+                                          P, P, c_int, P, P, P, P, P, P, c_size_t, P, P]
+    lib.t2va_stage3_objective.restype = c_int
+
+
+def load(path: Optional[str] = None):
+    """The loaded libt2va.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        p = path or LIB
+        if not os.path.exists(p):
+            raise RuntimeError(f"libt2va.so not found at {p}: build it with "
+                               f"`python -m joint_video_audio_02_b300.build`")
+        lib = ctypes.CDLL(p)
+        _declare(lib)
+        _LIB = lib
+    return _LIB
+
+
+def error_string(code: int) -> str:
+    return load().t2va_error_string(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise T2VAError(code, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return T2VA_BFLOAT16
+    if dt == torch.float32:
+        return T2VA_FLOAT32
+    raise TypeError(f"unsupported latent dtype {dt}")
+
+
+def _segments(groups: Sequence[Sequence[torch.Tensor]], batch: int):
+    """Geometry per modality, checked to be shared by every tensor of that modality."""
+    M = len(groups[0])
+    segs = (Segment * M)()
+    for m in range(M):
+        ref = groups[0][m]
+        for grp in groups:
+            x = grp[m]
+            if not x.is_cuda:
+                raise ValueError("every latent must be a CUDA tensor")
+            if x.shape[0] != batch:
+                raise ValueError("first dimension must be the batch")
+            if batch > 0 and x.dim() > 1 and not x[0].is_contiguous():
+                raise ValueError("each sample's elements must be contiguous")
+            if x.shape[1:] != ref.shape[1:] or (batch > 1 and x.stride(0) != ref.stride(0)):
+                raise ValueError("all tensors of one modality must share shape and sample stride")
+        n = 1
+        for d in ref.shape[1:]:
+            n *= int(d)
+        segs[m].numel = n
+        segs[m].sample_stride = int(ref.stride(0)) if batch > 1 else n
+    return segs
+
+
+def _ptrs(ts: Sequence[torch.Tensor]):
+    return (c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+
+
+def _opt(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _f32(t: torch.Tensor, name: str):
+    if t.dtype != torch.float32 or not t.is_cuda:
+        raise TypeError(f"{name} must be a float32 CUDA tensor")
+
+
+def workspace_bytes(batch: int, num_modalities: int) -> int:
+    n = load().t2va_workspace_bytes(int(batch), int(num_modalities))
+    if n == 0:
+        raise T2VAError(1, "t2va_workspace_bytes")
+    return int(n)
+
+
+def workspace_init(workspace: torch.Tensor, timeout_ms: int = 1000, stream=None):
+    _check(load().t2va_workspace_init(workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                      int(timeout_ms), _stream(stream)), "t2va_workspace_init")
+
+
+def new_workspace(batch: int, num_modalities: int, device=None, timeout_ms: int = 1000, stream=None):
+    """Allocate (through torch) and initialise a workspace for the objective calls."""
+    ws = torch.empty(workspace_bytes(batch, num_modalities), dtype=torch.uint8,
+                     device=device or torch.device("cuda"))
+    workspace_init(ws, timeout_ms, stream)
+    return ws
+
+
+def noise(z0: Sequence[torch.Tensor], eps: Sequence[torch.Tensor], zt: Sequence[torch.Tensor],
+          t: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None):
+    """z_t = cos(t) z0 + sin(t) eps per modality, into `zt` (t2va_noise)."""
+    B, M = int(t.shape[0]), len(z0)
+    segs = _segments([z0, eps, zt], B)
+    dt = _dtype_code(z0[0].dtype)
+    _f32(t, "t")
+    _check(load().t2va_noise(B, M, segs, dt, _ptrs(z0), _ptrs(eps), _ptrs(zt), t.data_ptr(),
+                             _opt(status), _stream(stream)), "t2va_noise")
+
+
+def scm_objective(z_t, x0_teacher, x0_student, x0_student_tangent, t, *, beta, gamma, eps_scm,
+                  weight, lambda_scm, grad_x0_student, loss, norm=None, accumulate=False,
+                  workspace, status, stream=None):
+    B, M = int(t.shape[0]), len(z_t)
+    segs = _segments([z_t, x0_teacher, x0_student, x0_student_tangent, grad_x0_student], B)
+    dt = _dtype_code(z_t[0].dtype)
+    for g in grad_x0_student:
+        _f32(g, "grad_x0_student")
+    w = (c_float * M)(*[float(x) for x in weight])
+    _check(load().t2va_scm_objective(
+        B, M, segs, dt, _ptrs(z_t), _ptrs(x0_teacher), _ptrs(x0_student), _ptrs(x0_student_tangent),
+        t.data_ptr(), float(beta), float(gamma), float(eps_scm), w, float(lambda_scm),
+        _ptrs(grad_x0_student), int(bool(accumulate)), loss.data_ptr(), _opt(norm),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), status.data_ptr(),
+        _stream(stream)), "t2va_scm_objective")
+
+
+def dmd_objective(zhat0, x0_teacher_hat, x0_fake, *, eps_dmd, weight, lambda_dmd, grad_zhat0, loss,
+                  cdmd=None, accumulate=False, workspace, status, stream=None):
+    B, M = int(zhat0[0].shape[0]), len(zhat0)
+    segs = _segments([zhat0, x0_teacher_hat, x0_fake, grad_zhat0], B)
+    dt = _dtype_code(zhat0[0].dtype)
+    for g in grad_zhat0:
+        _f32(g, "grad_zhat0")
+    w = (c_float * M)(*[float(x) for x in weight])
+    _check(load().t2va_dmd_objective(
+        B, M, segs, dt, _ptrs(zhat0), _ptrs(x0_teacher_hat), _ptrs(x0_fake), float(eps_dmd), w,
+        float(lambda_dmd), _ptrs(grad_zhat0), int(bool(accumulate)), loss.data_ptr(), _opt(cdmd),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), status.data_ptr(),
+        _stream(stream)), "t2va_dmd_objective")
+
+
+def stage3_objective(z_t, x0_teacher, x0_student, x0_student_tangent, t, zhat0, x0_teacher_hat,
+                     x0_fake, *, beta, gamma, eps_scm, eps_dmd, weight, lambda_scm, lambda_dmd,
+                     grad_x0_student, grad_zhat0, loss, loss_scm=None, loss_dmd=None, norm=None,
+                     cdmd=None, accumulate=False, workspace, status, stream=None):
+    B, M = int(t.shape[0]), len(z_t)
+    segs = _segments([z_t, x0_teacher, x0_student, x0_student_tangent, zhat0, x0_teacher_hat,
+                      x0_fake, grad_x0_student, grad_zhat0], B)
+    dt = _dtype_code(z_t[0].dtype)
+    for g in list(grad_x0_student) + list(grad_zhat0):
+        _f32(g, "gradient")
+    w = (c_float * M)(*[float(x) for x in weight])
+    _check(load().t2va_stage3_objective(
+        B, M, segs, dt, _ptrs(z_t), _ptrs(x0_teacher), _ptrs(x0_student), _ptrs(x0_student_tangent),
+        t.data_ptr(), _ptrs(zhat0), _ptrs(x0_teacher_hat), _ptrs(x0_fake),
+        float(beta), float(gamma), float(eps_scm), float(eps_dmd), w, float(lambda_scm),
+        float(lambda_dmd), _ptrs(grad_x0_student), _ptrs(grad_zhat0), int(bool(accumulate)),
+        loss.data_ptr(), _opt(loss_scm), _opt(loss_dmd), _opt(norm), _opt(cdmd),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), status.data_ptr(),
+        _stream(stream)), "t2va_stage3_objective")

@@ -1,0 +1,357 @@
+// C-ABI entry points of the joint video-audio distillation objective library.
+// Argument checking, device queries and launch planning; the arithmetic lives
+// in t2va_noise.cu and t2va_objective.cu. Declarations and the contract of
+// every entry point are in include/t2va.h.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "t2va_internal.cuh"
+
+using namespace t2va;
+
+namespace {
+
+struct DeviceInfo {
+  int sm_count = 0;
+  size_t smem_optin = 0;
+  bool valid = false;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mu;
+
+bool current_device(DeviceInfo* out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return false;
+  }
+  std::lock_guard<std::mutex> lock(g_devices_mu);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.valid) {
+    int sms = 0, optin = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    d.sm_count = sms;
+    d.smem_optin = (size_t)optin;
+    d.valid = sms > 0;
+  }
+  *out = d;
+  return d.valid;
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+inline bool finite(float x) { return std::isfinite(x); }
+
+int check_geometry(int B, int M, const t2va_segment* seg) {
+  if (B < 0 || M < 1 || M > kMaxM || seg == nullptr) return T2VA_ERROR_INVALID_ARGUMENT;
+  for (int m = 0; m < M; ++m) {
+    const int64_t n = seg[m].numel, s = seg[m].sample_stride;
+    if (n < 0 || s < 0) return T2VA_ERROR_INVALID_ARGUMENT;
+    if (B > 1 && s < n) return T2VA_ERROR_INVALID_ARGUMENT;
+    // every element offset must stay far from int64 overflow (x 8 bytes)
+    const int64_t lim = INT64_MAX / 16;
+    if (n > lim || (B > 1 && s > (lim - n) / (B - 1))) return T2VA_ERROR_INVALID_ARGUMENT;
+  }
+  return T2VA_SUCCESS;
+}
+
+int check_ptrs(int M, const t2va_segment* seg, const void* const* p) {
+  if (p == nullptr) return T2VA_ERROR_INVALID_ARGUMENT;
+  for (int m = 0; m < M; ++m) {
+    if (seg[m].numel > 0 && p[m] == nullptr) return T2VA_ERROR_INVALID_ARGUMENT;
+    if (!aligned(p[m], 16)) return T2VA_ERROR_MISALIGNED;
+  }
+  return T2VA_SUCCESS;
+}
+
+int check_dtype(t2va_dtype dt) {
+  return (dt == T2VA_FLOAT32 || dt == T2VA_BFLOAT16) ? T2VA_SUCCESS : T2VA_ERROR_UNSUPPORTED_DTYPE;
+}
+
+int check_weights(int M, const float* w) {
+  if (w == nullptr) return T2VA_ERROR_INVALID_ARGUMENT;
+  for (int m = 0; m < M; ++m)
+    if (!finite(w[m]) || w[m] < 0.f) return T2VA_ERROR_INVALID_ARGUMENT;
+  return T2VA_SUCCESS;
+}
+
+int check_scalar_out(const void* p, bool required) {
+  if (p == nullptr) return required ? T2VA_ERROR_INVALID_ARGUMENT : T2VA_SUCCESS;
+  return aligned(p, 4) ? T2VA_SUCCESS : T2VA_ERROR_MISALIGNED;
+}
+
+#define T2VA_TRY(expr)              \
+  do {                              \
+    const int rc_ = (expr);         \
+    if (rc_ != T2VA_SUCCESS) return rc_; \
+  } while (0)
+
+// Shared tail of the three objective entry points.
+int run_objective(ObjectiveArgs& a, t2va_dtype dt, int mode, void* workspace, size_t ws_size,
+                  cudaStream_t stream) {
+  DeviceInfo dev;
+  if (!current_device(&dev)) return T2VA_ERROR_CUDA;
+  const size_t need = ws_bytes(a.B, a.M, dev.sm_count);
+  if (workspace == nullptr || !aligned(workspace, 16) || ws_size < need) return T2VA_ERROR_WORKSPACE;
+  unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
+  a.hdr = reinterpret_cast<WsHeader*>(ws);
+  a.sync = reinterpret_cast<uint32_t*>(ws + kWsHeaderBytes);
+  a.partials = reinterpret_cast<float*>(ws + ws_partials_offset(a.B));
+  a.gmax = dev.sm_count;
+  ObjectiveLaunch l;
+  if (!plan_objective(a, dt, mode, dev.sm_count, dev.smem_optin, &l)) return T2VA_ERROR_CUDA;
+  const cudaError_t e = launch_objective(a, dt, mode, l, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return T2VA_ERROR_CUDA;
+  }
+  return T2VA_SUCCESS;
+}
+
+void fill_geometry(ObjectiveArgs& a, int B, int M, const t2va_segment* seg) {
+  std::memset(&a, 0, sizeof(a));
+  a.B = B;
+  a.M = M;
+  for (int m = 0; m < M; ++m) {
+    a.n[m] = seg[m].numel;
+    a.stride[m] = seg[m].sample_stride;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* t2va_error_string(int code) {
+  switch (code) {
+    case T2VA_SUCCESS: return "success";
+    case T2VA_ERROR_INVALID_ARGUMENT: return "invalid argument (size, scalar or null pointer)";
+    case T2VA_ERROR_UNSUPPORTED_DTYPE: return "unsupported dtype (float32 and bfloat16 only)";
+    case T2VA_ERROR_MISALIGNED: return "device pointer not 16-byte aligned (4-byte for scalars)";
+    case T2VA_ERROR_WORKSPACE: return "workspace null, misaligned or smaller than t2va_workspace_bytes()";
+    case T2VA_ERROR_CUDA: return "CUDA runtime error or kernel launch failure";
+    default: return "unknown t2va error code";
+  }
+}
+
+int t2va_abi_version(void) { return T2VA_ABI_VERSION; }
+
+size_t t2va_workspace_bytes(int batch, int num_modalities) {
+  if (batch < 0 || num_modalities < 1 || num_modalities > kMaxM) return 0;
+  DeviceInfo dev;
+  if (!current_device(&dev)) return 0;
+  return ws_bytes(batch, num_modalities, dev.sm_count);
+}
+
+int t2va_workspace_init(void* workspace, size_t workspace_bytes, uint32_t timeout_ms,
+                        cudaStream_t stream) {
+  if (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < kWsHeaderBytes)
+    return T2VA_ERROR_WORKSPACE;
+  DeviceInfo dev;
+  if (!current_device(&dev)) return T2VA_ERROR_CUDA;
+  const uint64_t ns = (uint64_t)(timeout_ms ? timeout_ms : 1000u) * 1000000ull;
+  if (launch_workspace_init(workspace, workspace_bytes, ns, (uint32_t)dev.sm_count, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return T2VA_ERROR_CUDA;
+  }
+  return T2VA_SUCCESS;
+}
+
+int t2va_noise(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+               const void* const* z0, const void* const* eps, void* const* zt,
+               const float* t, int* status, cudaStream_t stream) {
+  T2VA_TRY(check_geometry(batch, num_modalities, seg));
+  T2VA_TRY(check_dtype(dtype));
+  T2VA_TRY(check_ptrs(num_modalities, seg, z0));
+  T2VA_TRY(check_ptrs(num_modalities, seg, eps));
+  T2VA_TRY(check_ptrs(num_modalities, seg, reinterpret_cast<const void* const*>(zt)));
+  T2VA_TRY(check_scalar_out(t, true));
+  T2VA_TRY(check_scalar_out(status, false));
+  if (batch == 0) return T2VA_SUCCESS;
+  NoiseArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.B = batch;
+  a.M = num_modalities;
+  a.t = t;
+  a.status = status;
+  const int VE = dtype == T2VA_BFLOAT16 ? 8 : 4;
+  const int64_t per_cta = noise_vectors_per_cta();
+  int64_t total = 0;
+  for (int m = 0; m < num_modalities; ++m) {
+    a.n[m] = seg[m].numel;
+    a.stride[m] = seg[m].sample_stride;
+    a.z0[m] = z0[m];
+    a.eps[m] = eps[m];
+    a.zt[m] = zt[m];
+    // CTAs per (sample, modality); an empty modality gets no CTA at all
+    const int64_t vec_ub = (seg[m].numel + VE - 1) / VE;
+    const int64_t chunks = (vec_ub + per_cta - 1) / per_cta;
+    if (chunks > INT32_MAX) return T2VA_ERROR_INVALID_ARGUMENT;
+    a.chunks[m] = chunks > 0 ? (int)chunks : 1;
+    a.block_off[m] = (int)total;
+    total += (int64_t)batch * chunks;
+    if (total > INT32_MAX) return T2VA_ERROR_INVALID_ARGUMENT;
+  }
+  for (int m = num_modalities; m <= kMaxM; ++m) {
+    if (m < kMaxM) a.chunks[m] = 1;
+    a.block_off[m] = (int)total;
+  }
+  if (total == 0) return T2VA_SUCCESS;
+  if (launch_noise(a, dtype, (int)total, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return T2VA_ERROR_CUDA;
+  }
+  return T2VA_SUCCESS;
+}
+
+int t2va_scm_objective(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+                       const void* const* z_t, const void* const* x0_teacher,
+                       const void* const* x0_student, const void* const* x0_student_tangent,
+                       const float* t, float beta, float gamma, float eps_scm,
+                       const float* weight, float lambda_scm,
+                       float* const* grad_x0_student, int accumulate,
+                       float* loss, float* norm,
+                       void* workspace, size_t workspace_bytes, int* status,
+                       cudaStream_t stream) {
+  const int M = num_modalities;
+  T2VA_TRY(check_geometry(batch, M, seg));
+  T2VA_TRY(check_dtype(dtype));
+  for (const void* const* p : {z_t, x0_teacher, x0_student, x0_student_tangent})
+    T2VA_TRY(check_ptrs(M, seg, p));
+  T2VA_TRY(check_ptrs(M, seg, reinterpret_cast<const void* const*>(grad_x0_student)));
+  T2VA_TRY(check_scalar_out(t, true));
+  T2VA_TRY(check_scalar_out(loss, true));
+  T2VA_TRY(check_scalar_out(norm, false));
+  T2VA_TRY(check_scalar_out(status, true));
+  T2VA_TRY(check_weights(M, weight));
+  if (!finite(beta) || !(gamma >= 0.f && gamma <= 1.f) || !finite(eps_scm) || !(eps_scm > 0.f) ||
+      !finite(lambda_scm))
+    return T2VA_ERROR_INVALID_ARGUMENT;
+  if (batch == 0) return T2VA_SUCCESS;
+  ObjectiveArgs a;
+  fill_geometry(a, batch, M, seg);
+  for (int m = 0; m < M; ++m) {
+    a.in[kZt][m] = z_t[m];
+    a.in[kXT][m] = x0_teacher[m];
+    a.in[kXS][m] = x0_student[m];
+    a.in[kXdot][m] = x0_student_tangent[m];
+    a.grad_s[m] = grad_x0_student[m];
+    a.w[m] = weight[m];
+  }
+  a.t = t;
+  a.beta = beta;
+  a.gamma = gamma;
+  a.eps_s = eps_scm;
+  a.lam_s = lambda_scm;
+  a.accumulate = accumulate ? 1 : 0;
+  a.loss = loss;
+  a.norm = norm;
+  a.status = status;
+  return run_objective(a, dtype, kModeScm, workspace, workspace_bytes, stream);
+}
+
+int t2va_dmd_objective(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+                       const void* const* zhat0, const void* const* x0_teacher_hat,
+                       const void* const* x0_fake, float eps_dmd, const float* weight,
+                       float lambda_dmd, float* const* grad_zhat0, int accumulate,
+                       float* loss, float* cdmd,
+                       void* workspace, size_t workspace_bytes, int* status,
+                       cudaStream_t stream) {
+  const int M = num_modalities;
+  T2VA_TRY(check_geometry(batch, M, seg));
+  T2VA_TRY(check_dtype(dtype));
+  for (const void* const* p : {zhat0, x0_teacher_hat, x0_fake}) T2VA_TRY(check_ptrs(M, seg, p));
+  T2VA_TRY(check_ptrs(M, seg, reinterpret_cast<const void* const*>(grad_zhat0)));
+  T2VA_TRY(check_scalar_out(loss, true));
+  T2VA_TRY(check_scalar_out(cdmd, false));
+  T2VA_TRY(check_scalar_out(status, true));
+  T2VA_TRY(check_weights(M, weight));
+  if (!finite(eps_dmd) || !(eps_dmd > 0.f) || !finite(lambda_dmd)) return T2VA_ERROR_INVALID_ARGUMENT;
+  if (batch == 0) return T2VA_SUCCESS;
+  ObjectiveArgs a;
+  fill_geometry(a, batch, M, seg);
+  for (int m = 0; m < M; ++m) {
+    a.in[kZh][m] = zhat0[m];
+    a.in[kYT][m] = x0_teacher_hat[m];
+    a.in[kYF][m] = x0_fake[m];
+    a.grad_d[m] = grad_zhat0[m];
+    a.w[m] = weight[m];
+  }
+  a.eps_d = eps_dmd;
+  a.lam_d = lambda_dmd;
+  a.accumulate = accumulate ? 1 : 0;
+  a.loss = loss;
+  a.cdmd = cdmd;
+  a.status = status;
+  return run_objective(a, dtype, kModeDmd, workspace, workspace_bytes, stream);
+}
+
+int t2va_stage3_objective(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+                          const void* const* z_t, const void* const* x0_teacher,
+                          const void* const* x0_student, const void* const* x0_student_tangent,
+                          const float* t,
+                          const void* const* zhat0, const void* const* x0_teacher_hat,
+                          const void* const* x0_fake,
+                          float beta, float gamma, float eps_scm, float eps_dmd,
+                          const float* weight, float lambda_scm, float lambda_dmd,
+                          float* const* grad_x0_student, float* const* grad_zhat0, int accumulate,
+                          float* loss, float* loss_scm, float* loss_dmd, float* norm, float* cdmd,
+                          void* workspace, size_t workspace_bytes, int* status,
+                          cudaStream_t stream) {
+  const int M = num_modalities;
+  T2VA_TRY(check_geometry(batch, M, seg));
+  T2VA_TRY(check_dtype(dtype));
+  for (const void* const* p : {z_t, x0_teacher, x0_student, x0_student_tangent, zhat0,
+                               x0_teacher_hat, x0_fake})
+    T2VA_TRY(check_ptrs(M, seg, p));
+  T2VA_TRY(check_ptrs(M, seg, reinterpret_cast<const void* const*>(grad_x0_student)));
+  T2VA_TRY(check_ptrs(M, seg, reinterpret_cast<const void* const*>(grad_zhat0)));
+  T2VA_TRY(check_scalar_out(t, true));
+  T2VA_TRY(check_scalar_out(loss, true));
+  for (const float* p : {loss_scm, loss_dmd, norm, cdmd}) T2VA_TRY(check_scalar_out(p, false));
+  T2VA_TRY(check_scalar_out(status, true));
+  T2VA_TRY(check_weights(M, weight));
+  if (!finite(beta) || !(gamma >= 0.f && gamma <= 1.f) || !finite(eps_scm) || !(eps_scm > 0.f) ||
+      !finite(lambda_scm) || !finite(eps_dmd) || !(eps_dmd > 0.f) || !finite(lambda_dmd))
+    return T2VA_ERROR_INVALID_ARGUMENT;
+  if (batch == 0) return T2VA_SUCCESS;
+  ObjectiveArgs a;
+  fill_geometry(a, batch, M, seg);
+  for (int m = 0; m < M; ++m) {
+    a.in[kZt][m] = z_t[m];
+    a.in[kXT][m] = x0_teacher[m];
+    a.in[kXS][m] = x0_student[m];
+    a.in[kXdot][m] = x0_student_tangent[m];
+    a.in[kZh][m] = zhat0[m];
+    a.in[kYT][m] = x0_teacher_hat[m];
+    a.in[kYF][m] = x0_fake[m];
+    a.grad_s[m] = grad_x0_student[m];
+    a.grad_d[m] = grad_zhat0[m];
+    if (grad_x0_student[m] == grad_zhat0[m]) a.alias_mask |= 1u << m;
+    a.w[m] = weight[m];
+  }
+  a.t = t;
+  a.beta = beta;
+  a.gamma = gamma;
+  a.eps_s = eps_scm;
+  a.lam_s = lambda_scm;
+  a.eps_d = eps_dmd;
+  a.lam_d = lambda_dmd;
+  a.accumulate = accumulate ? 1 : 0;
+  a.loss = loss;
+  a.loss_s = loss_scm;
+  a.loss_d = loss_dmd;
+  a.norm = norm;
+  a.cdmd = cdmd;
+  a.status = status;
+  return run_objective(a, dtype, kModeStage3, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"

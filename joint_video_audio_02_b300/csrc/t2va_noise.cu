@@ -1,0 +1,127 @@
+// TrigFlow noising kernel: z_t = cos(t) z0 + sin(t) eps per modality, with one
+// timestep per sample shared by all modalities (TurboT2VA, section 三 of the
+// robotworld.top/zh reading: the noising equation; section 2 of the
+// robotworld.top/en summary).
+//
+// HBM-bound stream: 2 reads + 1 write per element. Each CTA owns one chunk of
+// one (sample, modality) segment, so the per-sample sin/cos is computed once per
+// thread and every access is a coalesced 16-byte vector; the few elements before
+// the first 16-byte boundary and after the last full vector of a segment are
+// done one by one by the first and last chunk.
+#include "t2va_internal.cuh"
+
+namespace t2va {
+namespace {
+
+constexpr int kNoiseThreads = 256;
+constexpr int kNoiseUnroll = 4;
+constexpr int kNoiseVecPerCta = kNoiseThreads * kNoiseUnroll;
+
+template <typename T>
+__device__ __forceinline__ void store_vec(void* p, const float* v);
+
+template <>
+__device__ __forceinline__ void store_vec<__nv_bfloat16>(void* p, const float* v) {
+  uint4 r;
+  __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]);
+  __nv_bfloat162 h1 = __floats2bfloat162_rn(v[2], v[3]);
+  __nv_bfloat162 h2 = __floats2bfloat162_rn(v[4], v[5]);
+  __nv_bfloat162 h3 = __floats2bfloat162_rn(v[6], v[7]);
+  r.x = *reinterpret_cast<uint32_t*>(&h0);
+  r.y = *reinterpret_cast<uint32_t*>(&h1);
+  r.z = *reinterpret_cast<uint32_t*>(&h2);
+  r.w = *reinterpret_cast<uint32_t*>(&h3);
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(r.x), "r"(r.y), "r"(r.z),
+               "r"(r.w)
+               : "memory");
+}
+
+template <>
+__device__ __forceinline__ void store_vec<float>(void* p, const float* v) {
+  asm volatile("st.global.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]),
+               "f"(v[3])
+               : "memory");
+}
+
+template <typename T>
+__device__ __forceinline__ void store_scalar(void* base, int64_t e, float v);
+template <>
+__device__ __forceinline__ void store_scalar<float>(void* base, int64_t e, float v) {
+  reinterpret_cast<float*>(base)[e] = v;
+}
+template <>
+__device__ __forceinline__ void store_scalar<__nv_bfloat16>(void* base, int64_t e, float v) {
+  reinterpret_cast<__nv_bfloat16*>(base)[e] = __float2bfloat16_rn(v);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kNoiseThreads) k_noise(const __grid_constant__ NoiseArgs a) {
+  constexpr int VE = Vec<T>::VE;
+  const int bid = blockIdx.x;
+  int m = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxM; ++i)
+    if (i < a.M && bid >= a.block_off[i]) m = i;
+  const int local = bid - a.block_off[m];
+  const int b = local / a.chunks[m];
+  const int chunk = local - b * a.chunks[m];
+
+  const float t = __ldg(a.t + b);
+  float s, c;
+  sincosf(t, &s, &c);
+  if (!isfinite(t) && a.status != nullptr && threadIdx.x == 0 && chunk == 0)
+    atomicOr(a.status, T2VA_STATUS_BAD_TIMESTEP);
+
+  const SegGeom g = seg_geom<VE>(a.n[m], a.stride[m], b);
+  const int64_t vec0 = g.e0 + g.head;  // element index of vector 0
+  const T* z0 = reinterpret_cast<const T*>(a.z0[m]);
+  const T* ep = reinterpret_cast<const T*>(a.eps[m]);
+  T* zt = reinterpret_cast<T*>(a.zt[m]);
+
+  const int64_t vbeg = (int64_t)chunk * kNoiseVecPerCta;
+  uint4 rz[kNoiseUnroll], re[kNoiseUnroll];
+#pragma unroll
+  for (int u = 0; u < kNoiseUnroll; ++u) {
+    const int64_t v = vbeg + u * kNoiseThreads + threadIdx.x;
+    if (v < g.nvec) {
+      rz[u] = ld_stream16(z0 + vec0 + v * VE);
+      re[u] = ld_stream16(ep + vec0 + v * VE);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kNoiseUnroll; ++u) {
+    const int64_t v = vbeg + u * kNoiseThreads + threadIdx.x;
+    if (v < g.nvec) {
+      Vec<T> vz, ve;
+      vz.from(rz[u]);
+      ve.from(re[u]);
+      float o[VE];
+#pragma unroll
+      for (int k = 0; k < VE; ++k) o[k] = fmaf(c, vz.v[k], s * ve.v[k]);
+      store_vec<T>(zt + vec0 + v * VE, o);
+    }
+  }
+  // unaligned head (first chunk) and tail (last chunk): one element per thread
+  if (chunk == 0 && threadIdx.x < g.head) {
+    const int64_t e = g.e0 + threadIdx.x;
+    store_scalar<T>(zt, e, fmaf(c, load_scalar<T>(z0, e), s * load_scalar<T>(ep, e)));
+  }
+  if (chunk == a.chunks[m] - 1 && threadIdx.x < g.tail) {
+    const int64_t e = vec0 + g.nvec * VE + threadIdx.x;
+    store_scalar<T>(zt, e, fmaf(c, load_scalar<T>(z0, e), s * load_scalar<T>(ep, e)));
+  }
+}
+
+}  // namespace
+
+int noise_vectors_per_cta() { return kNoiseVecPerCta; }
+
+cudaError_t launch_noise(const NoiseArgs& a, t2va_dtype dt, int grid, cudaStream_t st) {
+  if (dt == T2VA_BFLOAT16)
+    k_noise<__nv_bfloat16><<<grid, kNoiseThreads, 0, st>>>(a);
+  else
+    k_noise<float><<<grid, kNoiseThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace t2va

@@ -1,0 +1,323 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the float64 oracle
+on the same seeded inputs, for every workload and the edge cases of the method.
+
+Tolerances are stated in tests/t2va_gpu_util.py: per-sample loss / norm / c_DMD
+relative 1e-5 (float32 inputs) or 1e-4 (bfloat16 inputs); gradients per sample
+max |gpu - oracle| <= 1e-3 max |oracle|; noise within one unit in the last place.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import joint_video_audio_02_b300 as t2va
+import oracle
+import synthetic as S
+from joint_video_audio_02_b300.build import build
+from t2va_gpu_util import (Params, alloc_like, compare, gpu_run, grads_like, oracle_run, select,
+                           to_device, to_host, ulp_diff_bf16, ulp_diff_f32)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build()
+    t2va.load()
+
+
+def _inputs(name, **kw):
+    return S.make_workload_inputs(S.workload(name), **kw)
+
+
+# --------------------------------------------------------------------------
+# the workloads
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny_scm_f32", "scm_512x768_bf16", "stage3_1024x1792_bf16"])
+def test_noise_parity(name):
+    wl = S.workload(name)
+    inp = _inputs(name)
+    z0 = to_device(inp.z0, wl.dtype)
+    eps = to_device(inp.eps, wl.dtype)
+    zt = alloc_like(z0)
+    t = torch.from_numpy(inp.t).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t2va.noise(z0, eps, zt, t, status=status)
+    got = to_host(zt, wl.dtype)
+    ref = oracle.noise(inp.z0, inp.eps, inp.t, wl.dtype)
+    for m in range(len(got)):
+        d = ulp_diff_bf16(got[m], ref[m]) if wl.dtype == "bf16" else ulp_diff_f32(got[m], ref[m])
+        assert d.max() <= 1, f"modality {m}: {d.max()} ulp"
+        assert (d > 0).mean() < 1e-3, f"modality {m}: {(d > 0).mean():.2e} of elements off by one ulp"
+    assert status.item() == 0
+
+
+@pytest.mark.parametrize("name", ["tiny_scm_f32", "scm_512x768_bf16"])
+def test_scm_parity(name):
+    wl = S.workload(name)
+    inp = _inputs(name)
+    gpu = gpu_run(inp, Params.of(wl), S.SCM)
+    ref = oracle_run(inp, Params.of(wl), S.SCM)
+    assert gpu["status"] == 0
+    compare(gpu, ref, wl.dtype, S.SCM)
+
+
+@pytest.mark.parametrize("name", ["stage3_512x768_bf16", "stage3_1024x1792_bf16",
+                                  "stage3_sweep_b1_bf16", "stage3_sweep_b4_bf16"])
+def test_stage3_parity(name):
+    wl = S.workload(name)
+    inp = _inputs(name)
+    gpu = gpu_run(inp, Params.of(wl), S.STAGE3)
+    ref = oracle_run(inp, Params.of(wl), S.STAGE3)
+    assert gpu["status"] == 0
+    compare(gpu, ref, wl.dtype, S.STAGE3)
+
+
+@pytest.mark.parametrize("batch", [16, 32])
+def test_stage3_sweep_full_size_sampled(batch):
+    """Full-size launch; the oracle recomputes a sample of the batch (first, middle, last)."""
+    wl = S.workload(f"stage3_sweep_b{batch}_bf16")
+    inp = _inputs(wl.name)
+    gpu = gpu_run(inp, Params.of(wl), S.STAGE3)
+    assert gpu["status"] == 0
+    samples = [0, batch // 2, batch - 1]
+    ref = oracle_run(S.slice_samples(inp, samples), Params.of(wl), S.STAGE3)
+    compare(select(gpu, samples), ref, wl.dtype, S.STAGE3)
+    assert np.all(np.isfinite(gpu["loss"]))
+
+
+def test_dmd_parity():
+    wl = S.workload("stage3_512x768_bf16")
+    inp = _inputs(wl.name)
+    gpu = gpu_run(inp, Params.of(wl), S.DMD)
+    ref = oracle_run(inp, Params.of(wl), S.DMD)
+    assert gpu["status"] == 0
+    compare(gpu, ref, wl.dtype, S.DMD)
+
+
+def test_stage3_two_large_samples_one_slot():
+    """Two 1024x1792 samples: their directions do not fit on chip together, so the
+    kernel runs with one shared-memory slot."""
+    inp = S.make_inputs(2, S.workload("stage3_1024x1792_bf16").numels, "bf16", S.STAGE3, seed=(103,))
+    p = Params()
+    compare(gpu_run(inp, p, S.STAGE3), oracle_run(inp, p, S.STAGE3), "bf16", S.STAGE3)
+
+
+def test_stage3_recompute_beyond_shared_memory():
+    """A 12M-element sample: part of each CTA's slice does not fit in shared memory and
+    is recomputed from the inputs in the write phase."""
+    inp = S.make_inputs(1, [12_000_000, 1000], "bf16", S.STAGE3, seed=(104,))
+    p = Params(weight=(1.0, 2.0))
+    compare(gpu_run(inp, p, S.STAGE3), oracle_run(inp, p, S.STAGE3), "bf16", S.STAGE3)
+
+
+# --------------------------------------------------------------------------
+# edge cases
+# --------------------------------------------------------------------------
+
+RAGGED = [
+    # (batch, numels, stride padding)
+    (3, [1, 7], 0),
+    (2, [9, 8191], 3),
+    (5, [100003, 5], 1),
+    (2, [0, 77], 0),
+    (1, [12345], 0),
+    (3, [1000, 17, 4096], 5),
+    (2, [33, 64, 1, 250001], 7),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("mode", [S.SCM, S.DMD, S.STAGE3])
+@pytest.mark.parametrize("case", RAGGED, ids=[f"B{b}-{'-'.join(map(str, n))}-p{p}" for b, n, p in RAGGED])
+def test_ragged(dtype, mode, case):
+    B, numels, pad = case
+    inp = S.make_inputs(B, numels, dtype, S.STAGE3, seed=(200, B, len(numels), pad))
+    p = Params(weight=tuple(1.0 + 0.5 * m for m in range(len(numels))), gamma=0.7, beta=1.2)
+    gpu = gpu_run(inp, p, mode, stride_pad=pad)
+    ref = oracle_run(inp, p, mode)
+    assert gpu["status"] == 0
+    compare(gpu, ref, dtype, mode)
+
+
+def test_empty_batch():
+    z = [torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")]
+    t = torch.empty((0,), device="cuda")
+    t2va.noise(z, z, [torch.empty_like(z[0])], t)
+    ws = t2va.new_workspace(1, 1)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    loss = torch.empty((0,), device="cuda")
+    g = [torch.empty((0, 64), device="cuda")]
+    t2va.stage3_objective(z, z, z, z, t, z, z, z, beta=1, gamma=0.5, eps_scm=1e-6, eps_dmd=1e-6,
+                          weight=[1.0], lambda_scm=1, lambda_dmd=1, grad_x0_student=g, grad_zhat0=g,
+                          loss=loss, workspace=ws, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+
+
+@pytest.mark.parametrize("mode", [S.SCM, S.STAGE3])
+def test_bad_timesteps(mode):
+    """t outside (0, pi/2): that sample's outputs are NaN and the status bit is set;
+    the other samples are unaffected."""
+    inp = S.make_inputs(6, [5000, 300], "bf16", S.STAGE3, seed=(300,))
+    t = np.array([0.5, 0.0, np.float32(math.pi / 2), np.nan, -0.3, 1.2], dtype=np.float32)
+    p = Params()
+    gpu = gpu_run(inp, p, mode, t_override=t)
+    ref = oracle_run(inp, p, mode, t_override=t)
+    assert gpu["status"] & t2va.STATUS_BAD_TIMESTEP
+    assert np.array_equal(np.isnan(gpu["loss"]), [False, True, True, True, True, False])
+    compare(gpu, ref, "bf16", mode)
+
+
+def test_zero_direction_is_exactly_zero():
+    """gamma = 1, student = teacher, zero tangent, fake = teacher: both directions vanish,
+    so every norm, loss and gradient is exactly 0 (closed form)."""
+    inp = S.make_inputs(3, [4099, 130], "bf16", S.STAGE3, seed=(301,))
+    inp.x0_student = [a.copy() for a in inp.x0_teacher]
+    inp.x0_tangent = [np.zeros_like(a) for a in inp.x0_tangent]
+    inp.x0_fake = [a.copy() for a in inp.x0_teacher_hat]
+    gpu = gpu_run(inp, Params(gamma=1.0, beta=0.8), S.STAGE3)
+    assert gpu["status"] == 0
+    for k in ("loss", "norm", "loss_scm", "loss_dmd"):
+        assert np.all(gpu[k] == 0.0), k
+    for g in gpu["grad_x0_student"] + gpu["grad_zhat0"]:
+        assert np.all(g == 0.0)
+    assert np.all(gpu["cdmd"] > 0)
+
+
+def test_accumulate():
+    inp = S.make_inputs(2, [20000, 333], "bf16", S.STAGE3, seed=(302,))
+    p = Params()
+    rng = np.random.default_rng(0)
+    prior = {"grad_x0_student": [rng.normal(size=a.shape).astype(np.float32) for a in inp.z0],
+             "grad_zhat0": [rng.normal(size=a.shape).astype(np.float32) for a in inp.z0]}
+    gpu = gpu_run(inp, p, S.STAGE3, accumulate_into=prior)
+    ref = oracle_run(inp, p, S.STAGE3)
+    for k in ("grad_x0_student", "grad_zhat0"):
+        ref[k] = [r + q.astype(np.float64) for r, q in zip(ref[k], prior[k])]
+    compare(gpu, ref, "bf16", S.STAGE3)
+
+
+def test_alias_sums_gradients():
+    """grad_zhat0 given as the same buffer as grad_x0_student: the two gradients are summed."""
+    inp = S.make_inputs(2, [20000, 333], "bf16", S.STAGE3, seed=(303,))
+    p = Params()
+    gpu = gpu_run(inp, p, S.STAGE3, alias=True)
+    ref = oracle_run(inp, p, S.STAGE3)
+    summed = [a + b for a, b in zip(ref["grad_x0_student"], ref["grad_zhat0"])]
+    ref["grad_x0_student"] = summed
+    ref["grad_zhat0"] = summed
+    compare(gpu, ref, "bf16", S.STAGE3)
+
+
+def test_reproducible_bitwise():
+    inp = _inputs("stage3_512x768_bf16")
+    p = Params.of(S.workload("stage3_512x768_bf16"))
+    a = gpu_run(inp, p, S.STAGE3)
+    b = gpu_run(inp, p, S.STAGE3)
+    for k in ("loss", "norm", "cdmd"):
+        assert np.array_equal(a[k], b[k])
+    for k in ("grad_x0_student", "grad_zhat0"):
+        for x, y in zip(a[k], b[k]):
+            assert np.array_equal(x, y)
+
+
+def test_cuda_graph_capture_matches_eager():
+    wl = S.workload("stage3_512x768_bf16")
+    inp = _inputs(wl.name)
+    p = Params.of(wl)
+    dt = wl.dtype
+    z0, eps, xT, xS, tan, zh, yT, yF = (to_device(getattr(inp, f), dt) for f in (
+        "z0", "eps", "x0_teacher", "x0_student", "x0_tangent", "zhat0", "x0_teacher_hat", "x0_fake"))
+    t = torch.from_numpy(inp.t).cuda()
+    zt = alloc_like(z0)
+    gS, gD = grads_like(z0), grads_like(z0)
+    loss = torch.zeros(wl.batch, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = t2va.new_workspace(wl.batch, 2)
+
+    def step():
+        t2va.noise(z0, eps, zt, t, status=st)
+        t2va.stage3_objective(zt, xT, xS, tan, t, zh, yT, yF, beta=p.beta, gamma=p.gamma,
+                              eps_scm=p.eps_scm, eps_dmd=p.eps_dmd, weight=p.weight,
+                              lambda_scm=p.lambda_scm, lambda_dmd=p.lambda_dmd, grad_x0_student=gS,
+                              grad_zhat0=gD, loss=loss, workspace=ws, status=st)
+
+    step()
+    torch.cuda.synchronize()
+    eager = (loss.clone(), [g.clone() for g in gS], [g.clone() for g in gD])
+    for g in gS + gD:
+        g.zero_()
+    loss.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(loss, eager[0])
+    for a, b in zip(gS + gD, eager[1] + eager[2]):
+        assert torch.equal(a, b)
+
+
+# --------------------------------------------------------------------------
+# failure detection: bounded waits, workspace checks (no fault, no hang)
+# --------------------------------------------------------------------------
+
+def test_timeout_sets_status_and_poisons_workspace():
+    """A corrupted arrival counter means no CTA ever sees the last arrival; every wait
+    gives up after the workspace's limit (200 ms here), sets TIMEOUT and returns. The
+    workspace then refuses work until it is initialised again."""
+    inp = S.make_inputs(2, [50000, 500], "bf16", S.STAGE3, seed=(400,))
+    p = Params()
+    ws = t2va.new_workspace(2, 2, timeout_ms=200)
+    torch.cuda.synchronize()
+    ws.view(torch.int32)[64] = 0x40000000   # sample 0's arrival counter
+    bad = gpu_run(inp, p, S.STAGE3, workspace=ws)
+    assert bad["status"] & t2va.STATUS_TIMEOUT
+    again = gpu_run(inp, p, S.STAGE3, workspace=ws)
+    assert again["status"] & t2va.STATUS_BAD_WORKSPACE
+    t2va.workspace_init(ws, 200)
+    good = gpu_run(inp, p, S.STAGE3, workspace=ws)
+    assert good["status"] == 0
+    compare(good, oracle_run(inp, p, S.STAGE3), "bf16", S.STAGE3)
+
+
+def test_uninitialised_workspace_is_refused():
+    inp = S.make_inputs(2, [5000, 50], "bf16", S.STAGE3, seed=(401,))
+    ws = torch.zeros(t2va.workspace_bytes(2, 2), dtype=torch.uint8, device="cuda")
+    out = gpu_run(inp, Params(), S.STAGE3, workspace=ws)
+    assert out["status"] & t2va.STATUS_BAD_WORKSPACE
+    assert np.all(np.isnan(out["loss"]))   # nothing was written
+
+
+def test_host_errors_on_device():
+    inp = S.make_inputs(2, [64, 16], "bf16", S.STAGE3, seed=(402,))
+    z = to_device(inp.z0, "bf16")
+    t = torch.from_numpy(inp.t).cuda()
+    ws = t2va.new_workspace(2, 2)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    loss = torch.zeros(2, device="cuda")
+    g = grads_like(z)
+    small = ws[: ws.numel() // 2]
+    with pytest.raises(t2va.T2VAError) as e:
+        t2va.scm_objective(z, z, z, z, t, beta=1, gamma=0.5, eps_scm=1e-6, weight=[1, 1], lambda_scm=1,
+                           grad_x0_student=g, loss=loss, workspace=small, status=st)
+    assert e.value.code == 4
+    with pytest.raises(t2va.T2VAError) as e:
+        t2va.scm_objective(z, z, z, z, t, beta=1, gamma=1.5, eps_scm=1e-6, weight=[1, 1], lambda_scm=1,
+                           grad_x0_student=g, loss=loss, workspace=ws, status=st)
+    assert e.value.code == 1
+    flat = torch.zeros(2 * 64 + 8, dtype=torch.bfloat16, device="cuda")
+    mis = [flat[1:129].view(2, 64), z[1]]
+    with pytest.raises(t2va.T2VAError) as e:
+        t2va.noise(mis, mis, mis, t)
+    assert e.value.code == 3
