@@ -116,26 +116,35 @@ def committed_traffic(workload: str):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
+    """SM clock and clock-event reasons sampled in a background thread (NVML, looked up
+    by the CUDA device's UUID), or by an `nvidia-smi -lms` subprocess if NVML fails."""
+
     REASONS = {
         0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
         0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
         0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
     }
+    SMI_FIELDS = "timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active"
 
-    def __init__(self, index: int, period_s: float = 0.005):
-        self.samples = []
+    def __init__(self, uuid: str, period_s: float = 0.005):
+        self.samples = []          # (wall time, sm MHz, reason bits)
         self.period = period_s
         self.stop_evt = threading.Event()
-        self.ok = False
+        self.error = ""
+        self.max_mhz = None
+        self.uuid = uuid
+        self.proc = None
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception:
-            self.max_mhz = None
+            pynvml.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+            self.mode = "nvml"
+        except Exception as e:  # fall back to nvidia-smi
+            self.error = f"nvml: {type(e).__name__}: {e}"[:160]
+            self.mode = "smi"
         self.thread = threading.Thread(target=self._run, daemon=True)
 
     def _run(self):
@@ -143,34 +152,69 @@ class ClockSampler:
             try:
                 mhz = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
                 rs = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                self.samples.append((time.perf_counter(), mhz, rs))
+                self.samples.append((time.time(), mhz, int(rs)))
             except Exception:
                 pass
             time.sleep(self.period)
 
     def start(self):
-        if self.ok:
+        if self.mode == "nvml":
             self.thread.start()
+            return
+        import subprocess
+        import tempfile
+        self.smi_out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.uuid, f"--query-gpu={self.SMI_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.smi_out, stderr=subprocess.DEVNULL)
+            time.sleep(0.5)
+        except Exception as e:
+            self.error += f"; smi: {e}"[:160]
+            self.proc = None
 
     def stop(self):
         self.stop_evt.set()
-        if self.ok:
+        if self.mode == "nvml":
             self.thread.join()
+            return
+        if self.proc is None:
+            return
+        import datetime
+        self.proc.terminate()
+        self.proc.wait()
+        self.smi_out.seek(0)
+        for line in self.smi_out:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 4:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                self.samples.append((ts, float(parts[1]), int(parts[3], 16)))
+                self.max_mhz = float(parts[2])
+            except Exception:
+                continue
+        os.unlink(self.smi_out.name)
 
     def summary(self, t0: float, t1: float) -> dict:
-        if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml_unavailable"], "samples": 0}
-        inside = [s for s in self.samples if t0 <= s[0] <= t1]
-        if not inside and self.samples:
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no_samples"],
+                    "samples": 0, "source": self.mode, "note": self.error}
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        n_inside = len(inside)
+        if not inside:   # region shorter than the sampling period: nearest sample
             mid = 0.5 * (t0 + t1)
-            inside = [min(self.samples, key=lambda s: abs(s[0] - mid))]
-        mhz = [s[1] for s in inside]
+            inside = [min(self.samples, key=lambda x: abs(x[0] - mid))]
         bits = 0
-        for s in inside:
-            bits |= s[2]
+        for x in inside:
+            bits |= x[2]
         reasons = sorted({name for b, name in self.REASONS.items() if bits & b and b != 0x1})
-        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(inside)}
+        out = {"sm_mhz": statistics.median([x[1] for x in inside]), "sm_max_mhz": self.max_mhz,
+               "reasons": reasons, "samples": n_inside, "source": self.mode}
+        if self.error:
+            out["note"] = self.error
+        return out
 
 
 # ---------------------------------------------------------------------------
@@ -242,11 +286,15 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
                                norm=d["norm"], workspace=ws, status=status, stream=stream)
 
     def noise(d, stream=None):
-        t2va.noise(d["z0"], d["eps"], d["zt"], d["t"], status=status, stream=stream)
+        # both noisings (z0 -> z_t and the on-policy zhat0 -> zhat_t) share the per-sample t,
+        # so they go to the library as one call over four latents
         if wl.mode == S.STAGE3:
-            t2va.noise(d["zhat0"], d["eps_hat"], d["zht"], d["t"], status=status, stream=stream)
+            t2va.noise(d["z0"] + d["zhat0"], d["eps"] + d["eps_hat"], d["zt"] + d["zht"], d["t"],
+                       status=status, stream=stream)
+        else:
+            t2va.noise(d["z0"], d["eps"], d["zt"], d["t"], status=status, stream=stream)
 
-    launches_per_step = (2 if wl.mode == S.STAGE3 else 1) + 1
+    launches_per_step = 2
 
     # capture: graph of S steps with external timing events around each objective launch
     K, W = args.steps, args.warmup
@@ -282,13 +330,17 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     g_warm = capture(W, False) if W > 0 else None
     torch.cuda.synchronize()
 
-    # warm-up steps
+    # clock ramp (the GPU leaves its idle clocks only under sustained load), then W warm-up steps
+    ramp_t0 = time.time()
     with torch.cuda.stream(cap_stream):
+        while time.time() - ramp_t0 < args.clock_ramp_seconds:
+            g_main.replay()
+            cap_stream.synchronize()
         if g_warm is not None:
             g_warm.replay()
     cap_stream.synchronize()
 
-    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler = ClockSampler("GPU-" + str(props.uuid))
     sampler.start()
     time.sleep(0.05)
     if dist is not None:
@@ -296,7 +348,7 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    h0 = time.perf_counter()
+    h0 = time.time()
     with torch.cuda.stream(cap_stream):
         t_start.record(cap_stream)
         for _ in range(reps):
@@ -306,7 +358,7 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
         t_end.record(cap_stream)
     cap_stream.synchronize()
     torch.cuda.synchronize()
-    h1 = time.perf_counter()
+    h1 = time.time()
     if dist is not None:
         dist.barrier()
     time.sleep(0.02)
@@ -344,7 +396,8 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
                    "parallelism": f"replicas x{world} (samples sharded by rank, no collective)",
                    "l2": f"rotating {R} input sets ({R * set_bytes / 2**20:.0f} MiB >= 3x L2 "
                          f"{l2 / 2**20:.0f} MiB): no step finds its inputs in L2",
-                   "timing": "CUDA graph replay; CUDA events on the launching stream"},
+                   "timing": "CUDA graph replay; CUDA events on the launching stream",
+                   "clock_ramp_s": args.clock_ramp_seconds},
         "elements_per_s": nb["elements"] * world * K / (elapsed_ms * 1e-3),
         "hbm_fraction_of_step": round(value / world / peak, 4),
         "roofline": {"kernel": "t2va stage-3 objective" if wl.mode == S.STAGE3 else "t2va sCM objective",
@@ -512,6 +565,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(S.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--clock-ramp-seconds", type=float, default=0.5,
+                    help="untimed load before the warm-up steps so the GPU leaves its idle clocks")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -127,13 +127,14 @@ def _segments(groups: Sequence[Sequence[torch.Tensor]], batch: int):
                 raise ValueError("first dimension must be the batch")
             if batch > 0 and x.dim() > 1 and not x[0].is_contiguous():
                 raise ValueError("each sample's elements must be contiguous")
-            if x.shape[1:] != ref.shape[1:] or (batch > 1 and x.stride(0) != ref.stride(0)):
+            empty = x.numel() == 0
+            if x.shape[1:] != ref.shape[1:] or (batch > 1 and not empty and x.stride(0) != ref.stride(0)):
                 raise ValueError("all tensors of one modality must share shape and sample stride")
         n = 1
         for d in ref.shape[1:]:
             n *= int(d)
         segs[m].numel = n
-        segs[m].sample_stride = int(ref.stride(0)) if batch > 1 else n
+        segs[m].sample_stride = int(ref.stride(0)) if (batch > 1 and n > 0) else n
     return segs
 
 

@@ -169,12 +169,12 @@ int t2va_noise(int batch, int num_modalities, const t2va_segment* seg, t2va_dtyp
                const float* t, int* status, cudaStream_t stream) {
   T2VA_TRY(check_geometry(batch, num_modalities, seg));
   T2VA_TRY(check_dtype(dtype));
+  if (batch == 0) return T2VA_SUCCESS;
   T2VA_TRY(check_ptrs(num_modalities, seg, z0));
   T2VA_TRY(check_ptrs(num_modalities, seg, eps));
   T2VA_TRY(check_ptrs(num_modalities, seg, reinterpret_cast<const void* const*>(zt)));
   T2VA_TRY(check_scalar_out(t, true));
   T2VA_TRY(check_scalar_out(status, false));
-  if (batch == 0) return T2VA_SUCCESS;
   NoiseArgs a;
   std::memset(&a, 0, sizeof(a));
   a.B = batch;
@@ -223,6 +223,7 @@ int t2va_scm_objective(int batch, int num_modalities, const t2va_segment* seg, t
   const int M = num_modalities;
   T2VA_TRY(check_geometry(batch, M, seg));
   T2VA_TRY(check_dtype(dtype));
+  if (batch == 0) return T2VA_SUCCESS;
   for (const void* const* p : {z_t, x0_teacher, x0_student, x0_student_tangent})
     T2VA_TRY(check_ptrs(M, seg, p));
   T2VA_TRY(check_ptrs(M, seg, reinterpret_cast<const void* const*>(grad_x0_student)));
@@ -234,7 +235,6 @@ int t2va_scm_objective(int batch, int num_modalities, const t2va_segment* seg, t
   if (!finite(beta) || !(gamma >= 0.f && gamma <= 1.f) || !finite(eps_scm) || !(eps_scm > 0.f) ||
       !finite(lambda_scm))
     return T2VA_ERROR_INVALID_ARGUMENT;
-  if (batch == 0) return T2VA_SUCCESS;
   ObjectiveArgs a;
   fill_geometry(a, batch, M, seg);
   for (int m = 0; m < M; ++m) {
@@ -267,6 +267,7 @@ int t2va_dmd_objective(int batch, int num_modalities, const t2va_segment* seg, t
   const int M = num_modalities;
   T2VA_TRY(check_geometry(batch, M, seg));
   T2VA_TRY(check_dtype(dtype));
+  if (batch == 0) return T2VA_SUCCESS;
   for (const void* const* p : {zhat0, x0_teacher_hat, x0_fake}) T2VA_TRY(check_ptrs(M, seg, p));
   T2VA_TRY(check_ptrs(M, seg, reinterpret_cast<const void* const*>(grad_zhat0)));
   T2VA_TRY(check_scalar_out(loss, true));
@@ -274,7 +275,6 @@ int t2va_dmd_objective(int batch, int num_modalities, const t2va_segment* seg, t
   T2VA_TRY(check_scalar_out(status, true));
   T2VA_TRY(check_weights(M, weight));
   if (!finite(eps_dmd) || !(eps_dmd > 0.f) || !finite(lambda_dmd)) return T2VA_ERROR_INVALID_ARGUMENT;
-  if (batch == 0) return T2VA_SUCCESS;
   ObjectiveArgs a;
   fill_geometry(a, batch, M, seg);
   for (int m = 0; m < M; ++m) {
@@ -308,6 +308,7 @@ int t2va_stage3_objective(int batch, int num_modalities, const t2va_segment* seg
   const int M = num_modalities;
   T2VA_TRY(check_geometry(batch, M, seg));
   T2VA_TRY(check_dtype(dtype));
+  if (batch == 0) return T2VA_SUCCESS;
   for (const void* const* p : {z_t, x0_teacher, x0_student, x0_student_tangent, zhat0,
                                x0_teacher_hat, x0_fake})
     T2VA_TRY(check_ptrs(M, seg, p));
@@ -321,7 +322,6 @@ int t2va_stage3_objective(int batch, int num_modalities, const t2va_segment* seg
   if (!finite(beta) || !(gamma >= 0.f && gamma <= 1.f) || !finite(eps_scm) || !(eps_scm > 0.f) ||
       !finite(lambda_scm) || !finite(eps_dmd) || !(eps_dmd > 0.f) || !finite(lambda_dmd))
     return T2VA_ERROR_INVALID_ARGUMENT;
-  if (batch == 0) return T2VA_SUCCESS;
   ObjectiveArgs a;
   fill_geometry(a, batch, M, seg);
   for (int m = 0; m < M; ++m) {

@@ -16,7 +16,7 @@ constexpr uint32_t kWsMagic = 0x54325641u;  // "T2VA"
 // ---------------------------------------------------------------------------
 // Workspace layout (caller-owned device memory, prepared by t2va_workspace_init)
 //   [0, 256)                header
-//   [256, 256 + 64*B)       per-sample barrier words: arrivals at +0, generation at +32
+//   [256, 256 + 64*B)       per-round arrival counters, one per 64 bytes (rounds <= B)
 //   then                    partial sums float[B][M][3][gmax]
 // ---------------------------------------------------------------------------
 struct WsHeader {
@@ -24,7 +24,8 @@ struct WsHeader {
   uint32_t poisoned;     // set by a kernel that timed out; refused until re-initialised
   uint64_t timeout_ns;
   uint32_t gmax;         // partial-sum slots per (sample, modality, quantity)
-  uint32_t pad[59];
+  uint32_t exit_count;   // CTAs that finished the current call; the last one resets the counters
+  uint32_t pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
@@ -67,12 +68,19 @@ struct ObjectiveArgs {
   float* norm;
   float* cdmd;
   WsHeader* hdr;
-  uint32_t* sync;              // 16 words per sample: [0] arrivals, [8] generation
+  uint32_t* sync;              // arrival counter of round r at sync[16 r]
   float* partials;
   int gmax;
   int* status;
-  int slots;                   // samples whose direction is held on chip at once (1 or 2)
-  int cap;                     // vectors per slot held in shared memory
+  // launch plan (filled by plan_objective)
+  int groups;                  // 2: round r+1 is read while round r waits; 1: no overlap
+  int spr;                     // samples per round
+  int rounds;
+  int64_t chunk[kMaxM];        // vectors of one (sample, modality) owned by each CTA
+  int iters[kMaxM];            // ceil(chunk / threads)
+  int64_t cap[kMaxM];          // vectors per (sample, modality) kept in shared memory
+  int64_t choff[kMaxM];        // float4 offset of modality m inside one sample's region
+  int64_t sample_f4;           // float4 per sample region
 };
 
 struct NoiseArgs {
@@ -97,8 +105,8 @@ struct ObjectiveLaunch {
   int threads;
   size_t smem;
 };
-// Chooses grid, slots and capacity for `a` (fills a.slots, a.cap); returns false
-// if the device cannot run it.
+// Chooses the grid and the round plan for `a` (fills the plan fields); returns
+// false if the device cannot run it.
 bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int mode, int sm_count, size_t smem_optin,
                     ObjectiveLaunch* out);
 cudaError_t launch_objective(const ObjectiveArgs& a, t2va_dtype dt, int mode,

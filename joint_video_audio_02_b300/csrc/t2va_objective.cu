@@ -3,25 +3,27 @@
 // robotworld.top/en summary: Eq. 6 and Eq. 11-12).
 //
 // Design (one persistent launch, one CTA per SM, all CTAs co-resident):
-//   for every sample b, every CTA owns a contiguous slice of that sample's
-//   16-byte vectors (video and audio segments back to back), so every sample is
-//   spread over the whole GPU and the small audio segment never idles SMs.
-//   Phase A(b): stream the slice's inputs once (16-byte loads), compute the
-//     float32 directions g_sCM and g_DMD, keep them in shared memory, and
-//     accumulate the per-(sample, modality) sums  sum g_sCM^2, sum |zhat0 - y_T|,
-//     sum g_DMD^2. The CTA's sums go to the workspace; then the CTA arrives on
-//     the sample's counter.
-//   Wait(b): a bounded spin on the sample's generation word; every CTA then
-//     merges the per-CTA sums itself in a fixed order (all CTAs get identical,
-//     run-to-run reproducible totals).
-//   Phase W(b): scale the kept directions by the per-(sample, modality) factor
-//     and write the float32 gradients once.
-//   With two shared-memory slots the order is A0 A1 W0 A2 W1 ... so sample b's
-//   barrier is hidden behind sample b+1's reads. Vectors that do not fit in
-//   shared memory are recomputed from the inputs in phase W.
-// HBM traffic is therefore the algorithmic minimum whenever the direction of
-// one (or two) samples fits on chip: each input read once, each gradient
-// written once.
+//   Every (sample, modality) segment is cut into G equal chunks of 16-byte vectors,
+//   one per CTA, so every segment is spread over the whole GPU and the small audio
+//   segment never leaves SMs idle. Samples are processed in rounds of `spr`
+//   samples that share one cross-CTA barrier:
+//   Phase A(r): stream the round's inputs once (16-byte loads, the next item's
+//     loads in flight while the current one computes), compute the float32
+//     directions g_sCM and g_DMD, keep them in shared memory, and accumulate the
+//     per-(sample, modality) sums  sum g_sCM^2, sum |zhat0 - y_T|, sum g_DMD^2.
+//     Each CTA writes its sums to the workspace and adds 1 to the round's counter.
+//   Wait(r): a bounded poll until the counter reaches G; every CTA then merges the
+//     per-CTA sums itself in a fixed order (identical, run-to-run reproducible
+//     totals in every CTA) and derives the per-(sample, modality) gradient factor.
+//   Phase W(r): scale the kept directions and write the float32 gradients once.
+//   With two shared-memory groups the order is A0 A1 W0 A2 W1 ... so each round's
+//   barrier is hidden behind the next round's reads. Vectors that do not fit in
+//   shared memory are recomputed from the inputs in phase W. The last CTA to
+//   finish resets the counters for the next call.
+// HBM traffic is therefore the algorithmic minimum whenever one sample's
+// directions fit on chip: each input read once, each gradient written once.
+#include <algorithm>
+
 #include "t2va_internal.cuh"
 
 namespace t2va {
@@ -29,13 +31,21 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 2;
+constexpr int kMaxRound = 8;  // samples per round
+
+struct RoundCoef {
+  float kD, kz, kx, s;
+  int ok;
+};
 
 struct SmemCtl {
-  float red[2][kWarps][kMaxM][kQuantities];
-  float tot[kMaxM][kQuantities];
+  float red[kWarps][kMaxRound][kMaxM][kQuantities];
+  float scal[kMaxRound][kMaxM][kQuantities];
+  float tot[2][kMaxRound][kMaxM][kQuantities];
+  float scaleS[2][kMaxRound][kMaxM];
+  float scaleD[2][kMaxRound][kMaxM];
+  RoundCoef coef[2][kMaxRound];
   uint64_t timeout_ns;
-  uint32_t gen_wait[2];
   int abort;
   int checked;
 };
@@ -46,8 +56,6 @@ struct Traits {
   static constexpr int VE = Vec<T>::VE;
   static constexpr bool kScm = (MODE & kModeScm) != 0;
   static constexpr bool kDmd = (MODE & kModeDmd) != 0;
-  static constexpr int Q = (kScm ? 1 : 0) + (kDmd ? 1 : 0);
-  static constexpr int P = Q * VE / 4;  // float4 pieces kept per vector
 };
 
 template <typename T, int MODE>
@@ -59,23 +67,22 @@ template <typename T, int MODE>
 __device__ __forceinline__ void load_vec(Loaded<T, MODE>& L, const ObjectiveArgs& a, int m,
                                          int64_t e) {
   using Tr = Traits<T, MODE>;
-  const T* p;
   if constexpr (Tr::kScm) {
-    p = reinterpret_cast<const T*>(a.in[kZt][m]); L.r[kZt] = ld_stream16(p + e);
-    p = reinterpret_cast<const T*>(a.in[kXT][m]); L.r[kXT] = ld_stream16(p + e);
-    p = reinterpret_cast<const T*>(a.in[kXS][m]); L.r[kXS] = ld_stream16(p + e);
-    p = reinterpret_cast<const T*>(a.in[kXdot][m]); L.r[kXdot] = ld_stream16(p + e);
+    L.r[kZt] = ld_stream16(reinterpret_cast<const T*>(a.in[kZt][m]) + e);
+    L.r[kXT] = ld_stream16(reinterpret_cast<const T*>(a.in[kXT][m]) + e);
+    L.r[kXS] = ld_stream16(reinterpret_cast<const T*>(a.in[kXS][m]) + e);
+    L.r[kXdot] = ld_stream16(reinterpret_cast<const T*>(a.in[kXdot][m]) + e);
   }
   if constexpr (Tr::kDmd) {
-    p = reinterpret_cast<const T*>(a.in[kZh][m]); L.r[kZh] = ld_stream16(p + e);
-    p = reinterpret_cast<const T*>(a.in[kYT][m]); L.r[kYT] = ld_stream16(p + e);
-    p = reinterpret_cast<const T*>(a.in[kYF][m]); L.r[kYF] = ld_stream16(p + e);
+    L.r[kZh] = ld_stream16(reinterpret_cast<const T*>(a.in[kZh][m]) + e);
+    L.r[kYT] = ld_stream16(reinterpret_cast<const T*>(a.in[kYT][m]) + e);
+    L.r[kYF] = ld_stream16(reinterpret_cast<const T*>(a.in[kYF][m]) + e);
   }
 }
 
 // Directions of one vector: gs (sCM) and gd (DMD), and the three sums.
 template <typename T, int MODE>
-__device__ __forceinline__ void directions(const Loaded<T, MODE>& L, const Coef& k,
+__device__ __forceinline__ void directions(const Loaded<T, MODE>& L, const RoundCoef& k,
                                            float* gs, float* gd, float& sg, float& sa,
                                            float& sd) {
   using Tr = Traits<T, MODE>;
@@ -108,10 +115,127 @@ __device__ __forceinline__ void directions(const Loaded<T, MODE>& L, const Coef&
   }
 }
 
-// One element, for the unaligned head and tail of a segment.
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float sum16(float v) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// One work item of a thread: vector k*threads + tid of this CTA's chunk of the
+// (sample b0 + bl, modality m) segment.
+struct Item {
+  int bl, m, k;
+};
+
+struct ItemInfo {
+  int64_t e;    // first element of the vector
+  int64_t pos;  // position inside the CTA's chunk (shared-memory slot)
+  bool valid;
+};
+
+// Advance to the next (bl, m, k) with k < iters[m]; false when the round is done.
+__device__ __forceinline__ bool next_item(Item& it, int nb, const ObjectiveArgs& a) {
+  if (++it.k < a.iters[it.m]) return true;
+  it.k = 0;
+  for (;;) {
+    if (++it.m == a.M) {
+      it.m = 0;
+      if (++it.bl == nb) return false;
+    }
+    if (a.iters[it.m] > 0) return true;
+  }
+}
+
+__device__ __forceinline__ bool first_item(Item& it, int nb, const ObjectiveArgs& a) {
+  it.bl = 0;
+  it.k = 0;
+  for (it.m = 0; it.m < a.M; ++it.m)
+    if (a.iters[it.m] > 0) return nb > 0;
+  return false;
+}
+
+template <int VE>
+__device__ __forceinline__ ItemInfo item_info(const Item& it, int b0, int cta, const ObjectiveArgs& a) {
+  const SegGeom g = seg_geom<VE>(a.n[it.m], a.stride[it.m], b0 + it.bl);
+  const int64_t chunk = a.chunk[it.m];
+  const int64_t lo = (int64_t)cta * chunk;
+  const int64_t pos = (int64_t)it.k * kThreads + threadIdx.x;
+  const int64_t v = lo + pos;
+  const int64_t vend = min(lo + chunk, g.nvec);
+  ItemInfo r;
+  r.valid = v < vend;
+  r.pos = pos;
+  r.e = g.e0 + g.head + v * VE;
+  return r;
+}
+
 template <typename T, int MODE>
-__device__ __forceinline__ void direction_scalar(const ObjectiveArgs& a, int m, int64_t e,
-                                                 const Coef& k, float& gs, float& gd) {
+__device__ __forceinline__ void keep(float4* region, int64_t cap, int64_t pos, const float* gs,
+                                     const float* gd) {
+  using Tr = Traits<T, MODE>;
+  constexpr int VE = Tr::VE;
+  int p = 0;
+  if constexpr (Tr::kScm) {
+#pragma unroll
+    for (int i = 0; i < VE; i += 4, ++p)
+      region[p * cap + pos] = make_float4(gs[i], gs[i + 1], gs[i + 2], gs[i + 3]);
+  }
+  if constexpr (Tr::kDmd) {
+#pragma unroll
+    for (int i = 0; i < VE; i += 4, ++p)
+      region[p * cap + pos] = make_float4(gd[i], gd[i + 1], gd[i + 2], gd[i + 3]);
+  }
+}
+
+template <typename T, int MODE>
+__device__ __forceinline__ void fetch(const float4* region, int64_t cap, int64_t pos, float* gs,
+                                      float* gd) {
+  using Tr = Traits<T, MODE>;
+  constexpr int VE = Tr::VE;
+  int p = 0;
+  if constexpr (Tr::kScm) {
+#pragma unroll
+    for (int i = 0; i < VE; i += 4, ++p) {
+      const float4 f = region[p * cap + pos];
+      gs[i] = f.x; gs[i + 1] = f.y; gs[i + 2] = f.z; gs[i + 3] = f.w;
+    }
+  }
+  if constexpr (Tr::kDmd) {
+#pragma unroll
+    for (int i = 0; i < VE; i += 4, ++p) {
+      const float4 f = region[p * cap + pos];
+      gd[i] = f.x; gd[i + 1] = f.y; gd[i + 2] = f.z; gd[i + 3] = f.w;
+    }
+  }
+}
+
+// The unaligned head and tail elements of every (sample, modality) segment of the
+// round are handled by CTA G-1, one element per thread: 16 threads per segment
+// (at most 7 head + 7 tail elements), at most kMaxRound * kMaxM = 32 segments.
+// Returns the element index, or -1 if this thread has none; sets the slot (bl, m).
+template <int VE>
+__device__ __forceinline__ int64_t scalar_element(const ObjectiveArgs& a, int b0, int nb, int& bl,
+                                                  int& m) {
+  const int pair = threadIdx.x >> 4, lane16 = threadIdx.x & 15;
+  bl = pair / a.M;
+  m = pair - bl * a.M;
+  if (bl >= nb) return -1;
+  const SegGeom g = seg_geom<VE>(a.n[m], a.stride[m], b0 + bl);
+  if (lane16 < g.head) return g.e0 + lane16;
+  if (lane16 >= 8 && lane16 - 8 < g.tail) return g.e0 + g.head + g.nvec * VE + (lane16 - 8);
+  return -1;
+}
+
+template <typename T, int MODE>
+__device__ __forceinline__ void scalar_direction(const ObjectiveArgs& a, int m, int64_t e,
+                                                 const RoundCoef& k, float& gs, float& gd,
+                                                 float& sabs) {
   using Tr = Traits<T, MODE>;
   if constexpr (Tr::kScm) {
     const float z = load_scalar<T>(a.in[kZt][m], e);
@@ -121,128 +245,94 @@ __device__ __forceinline__ void direction_scalar(const ObjectiveArgs& a, int m, 
     gs = fmaf(k.kD, xt - xs, fmaf(k.kz, z, k.kx * xd));
   }
   if constexpr (Tr::kDmd) {
+    const float zh = load_scalar<T>(a.in[kZh][m], e);
     const float yt = load_scalar<T>(a.in[kYT][m], e);
     const float yf = load_scalar<T>(a.in[kYF][m], e);
     gd = yf - yt;
+    sabs = fabsf(zh - yt);
   }
 }
 
 template <typename T, int MODE>
-__device__ __forceinline__ float abs_residual_scalar(const ObjectiveArgs& a, int m, int64_t e) {
-  const float zh = load_scalar<T>(a.in[kZh][m], e);
-  const float yt = load_scalar<T>(a.in[kYT][m], e);
-  return fabsf(zh - yt);
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Per-sample vector index space: modality 0's aligned vectors, then modality 1's, ...
-template <int VE>
-__device__ __forceinline__ int64_t sample_vectors(const ObjectiveArgs& a, int b) {
-  int64_t v = 0;
-  for (int m = 0; m < a.M; ++m) v += seg_geom<VE>(a.n[m], a.stride[m], b).nvec;
-  return v;
-}
-
-__device__ __forceinline__ int scalar_owner(int b, int m, int M, int G) {
-  return (int)(((int64_t)b * M + m) % G);
-}
-
-template <typename T, int MODE>
-__device__ void phase_a(const ObjectiveArgs& a, SmemCtl& ctl, float4* slot, int b, int cta, int G) {
+__device__ void phase_a(const ObjectiveArgs& a, SmemCtl& ctl, float4* group, int r, int cta, int G) {
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int par = b & 1;
-  const int64_t V = sample_vectors<VE>(a, b);
-  const int64_t lo = V * cta / G, hi = V * (cta + 1) / G;
-  const Coef k = Tr::kScm ? sample_coef(__ldg(a.t + b), a.beta, a.gamma) : Coef{};
+  const int gi = r % a.groups;
+  const int b0 = r * a.spr;
+  const int nb = min(a.spr, a.B - b0);
 
-  int64_t voff = 0;
-  for (int m = 0; m < a.M; ++m) {
-    float sg = 0.f, sa = 0.f, sd = 0.f;
-    const SegGeom g = seg_geom<VE>(a.n[m], a.stride[m], b);
-    const int64_t a0 = max(lo, voff), a1 = min(hi, voff + g.nvec);
-    const int64_t ebase = g.e0 + g.head - voff * VE;  // element of vector v is ebase + v*VE
-    voff += g.nvec;
-    for (int64_t v = a0 + tid; v < a1; v += kThreads * kUnroll) {
-      const int64_t v1 = v + kThreads;
-      const bool has1 = v1 < a1;
-      Loaded<T, MODE> L0, L1;
-      load_vec<T, MODE>(L0, a, m, ebase + v * VE);
-      if (has1) load_vec<T, MODE>(L1, a, m, ebase + v1 * VE);
-      {
-        float gs[VE], gd[VE];
-        directions<T, MODE>(L0, k, gs, gd, sg, sa, sd);
-        const int64_t pos = v - lo;
-        if (pos < a.cap) {
-          float4* dst = slot + pos;
-          int p = 0;
-          if constexpr (Tr::kScm) {
-#pragma unroll
-            for (int i = 0; i < VE; i += 4, ++p)
-              dst[(int64_t)p * a.cap] = make_float4(gs[i], gs[i + 1], gs[i + 2], gs[i + 3]);
-          }
-          if constexpr (Tr::kDmd) {
-#pragma unroll
-            for (int i = 0; i < VE; i += 4, ++p)
-              dst[(int64_t)p * a.cap] = make_float4(gd[i], gd[i + 1], gd[i + 2], gd[i + 3]);
-          }
-        }
-      }
-      if (has1) {
-        float gs[VE], gd[VE];
-        directions<T, MODE>(L1, k, gs, gd, sg, sa, sd);
-        const int64_t pos = v1 - lo;
-        if (pos < a.cap) {
-          float4* dst = slot + pos;
-          int p = 0;
-          if constexpr (Tr::kScm) {
-#pragma unroll
-            for (int i = 0; i < VE; i += 4, ++p)
-              dst[(int64_t)p * a.cap] = make_float4(gs[i], gs[i + 1], gs[i + 2], gs[i + 3]);
-          }
-          if constexpr (Tr::kDmd) {
-#pragma unroll
-            for (int i = 0; i < VE; i += 4, ++p)
-              dst[(int64_t)p * a.cap] = make_float4(gd[i], gd[i + 1], gd[i + 2], gd[i + 3]);
-          }
-        }
-      }
+  if (r >= a.groups) __syncthreads();  // this group's buffers were last read in W(r - groups)
+  if (tid < nb) {
+    RoundCoef c{0.f, 0.f, 0.f, 1.f, 1};
+    if constexpr (Tr::kScm) {
+      const Coef k = sample_coef(__ldg(a.t + b0 + tid), a.beta, a.gamma);
+      c = RoundCoef{k.kD, k.kz, k.kx, k.s, k.ok ? 1 : 0};
     }
-    // unaligned head/tail elements of this (sample, modality): warp 0 of the owner CTA
-    if (warp == 0 && cta == scalar_owner(b, m, a.M, G)) {
-      int64_t e = -1;
-      if (lane < g.head) e = g.e0 + lane;
-      else if (lane >= 8 && lane - 8 < g.tail) e = g.e0 + g.head + g.nvec * VE + (lane - 8);
-      if (e >= 0) {
-        float gs = 0.f, gd = 0.f;
-        direction_scalar<T, MODE>(a, m, e, k, gs, gd);
-        if constexpr (Tr::kScm) sg = fmaf(gs, gs, sg);
-        if constexpr (Tr::kDmd) {
-          sd = fmaf(gd, gd, sd);
-          sa += abs_residual_scalar<T, MODE>(a, m, e);
-        }
-      }
-    }
-    sg = warp_sum(sg);
-    sa = warp_sum(sa);
-    sd = warp_sum(sd);
-    if (lane == 0) {
-      ctl.red[par][warp][m][0] = sg;
-      ctl.red[par][warp][m][1] = sa;
-      ctl.red[par][warp][m][2] = sd;
-    }
+    ctl.coef[gi][tid] = c;
   }
   __syncthreads();
 
-  // CTA sums -> workspace, then arrive on the sample's counter.
+  // unaligned head/tail elements (CTA G-1 only; block-uniform branch)
+  if (cta == G - 1) {
+    int bl, m;
+    const int64_t e = scalar_element<VE>(a, b0, nb, bl, m);
+    float gs = 0.f, gd = 0.f, sabs = 0.f;
+    if (e >= 0) scalar_direction<T, MODE>(a, m, e, ctl.coef[gi][bl], gs, gd, sabs);
+    const float sg = sum16(gs * gs), sa = sum16(sabs), sd = sum16(gd * gd);
+    if ((tid & 15) == 0 && bl < nb) {
+      ctl.scal[bl][m][0] = sg;
+      ctl.scal[bl][m][1] = sa;
+      ctl.scal[bl][m][2] = sd;
+    }
+  }
+
+  // this CTA's vectors of every segment of the round; the next item's loads are in
+  // flight while the current item is computed
+  Item it;
+  bool more = first_item(it, nb, a);
+  Loaded<T, MODE> Lc;
+  ItemInfo ic{0, 0, false};
+  if (more) {
+    ic = item_info<VE>(it, b0, cta, a);
+    if (ic.valid) load_vec<T, MODE>(Lc, a, it.m, ic.e);
+  }
+  float sg = 0.f, sa = 0.f, sd = 0.f;
+  while (more) {
+    Item nx = it;
+    const bool more_n = next_item(nx, nb, a);
+    Loaded<T, MODE> Ln;
+    ItemInfo in{0, 0, false};
+    if (more_n) {
+      in = item_info<VE>(nx, b0, cta, a);
+      if (in.valid) load_vec<T, MODE>(Ln, a, nx.m, in.e);
+    }
+    if (ic.valid) {
+      float gs[VE], gd[VE];
+      directions<T, MODE>(Lc, ctl.coef[gi][it.bl], gs, gd, sg, sa, sd);
+      if (ic.pos < a.cap[it.m])
+        keep<T, MODE>(group + it.bl * a.sample_f4 + a.choff[it.m], a.cap[it.m], ic.pos, gs, gd);
+    }
+    if (!more_n || nx.bl != it.bl || nx.m != it.m) {  // end of a segment (warp-uniform)
+      sg = warp_sum(sg);
+      sa = warp_sum(sa);
+      sd = warp_sum(sd);
+      if (lane == 0) {
+        ctl.red[warp][it.bl][it.m][0] = sg;
+        ctl.red[warp][it.bl][it.m][1] = sa;
+        ctl.red[warp][it.bl][it.m][2] = sd;
+      }
+      sg = sa = sd = 0.f;
+    }
+    it = nx;
+    ic = in;
+    Lc = Ln;
+    more = more_n;
+  }
+  __syncthreads();
+
+  // CTA sums -> workspace, then one arrival on the round's counter (no wait here)
   if (warp == 0) {
-    const int nq = a.M * kQuantities;
     if (tid == 0 && !ctl.checked) {
       const uint32_t magic = ld_relaxed_gpu(&a.hdr->magic);
       const uint32_t poisoned = ld_relaxed_gpu(&a.hdr->poisoned);
@@ -254,41 +344,42 @@ __device__ void phase_a(const ObjectiveArgs& a, SmemCtl& ctl, float4* slot, int 
       }
     }
     __syncwarp();
-    const bool abort = ctl.abort != 0;
-    if (!abort && lane < nq) {
-      const int m = lane / kQuantities, q = lane - m * kQuantities;
-      float s = 0.f;
+    if (!ctl.abort) {
+      const int per_bl = a.M * kQuantities;
+      for (int u = lane; u < nb * per_bl; u += 32) {
+        const int bl = u / per_bl;
+        const int m = (u - bl * per_bl) / kQuantities;
+        const int q = u - bl * per_bl - m * kQuantities;
+        float s = 0.f;
+        if (a.iters[m] > 0) {
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) s += ctl.red[par][w][m][q];
-      a.partials[((int64_t)(b * a.M + m) * kQuantities + q) * a.gmax + cta] = s;
-      __threadfence();
-    }
-    __syncwarp();
-    if (lane == 0 && !abort) {
-      uint32_t* cnt = a.sync + (int64_t)b * 16;
-      uint32_t* gen = cnt + 8;
-      const uint32_t g0 = ld_relaxed_gpu(gen);
-      ctl.gen_wait[par] = g0;
-      __threadfence();
-      const uint32_t old = atomicAdd(cnt, 1u);
-      if (old == (uint32_t)(G - 1)) {
-        *reinterpret_cast<volatile uint32_t*>(cnt) = 0u;
+          for (int w = 0; w < kWarps; ++w) s += ctl.red[w][bl][m][q];
+        }
+        if (cta == G - 1) s += ctl.scal[bl][m][q];
+        a.partials[(((int64_t)(b0 + bl) * a.M + m) * kQuantities + q) * a.gmax + cta] = s;
+      }
+      __syncwarp();
+      if (lane == 0) {
         __threadfence();
-        st_release_gpu(gen, g0 + 1u);
+        atomicAdd(a.sync + (int64_t)r * 16, 1u);
       }
     }
   }
 }
 
-// Bounded wait for every CTA's sums of sample b, then the fixed-order merge.
-template <int MODE>
-__device__ bool wait_and_merge(const ObjectiveArgs& a, SmemCtl& ctl, int b, int G) {
+// Bounded wait for every CTA's sums of round r, then the fixed-order merge and the
+// per-(sample, modality) gradient factors.
+template <typename T, int MODE>
+__device__ bool wait_and_merge(const ObjectiveArgs& a, SmemCtl& ctl, int r, int G) {
+  using Tr = Traits<T, MODE>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gi = r % a.groups;
+  const int b0 = r * a.spr;
+  const int nb = min(a.spr, a.B - b0);
   if (tid == 0 && !ctl.abort) {
-    const uint32_t* gen = a.sync + (int64_t)b * 16 + 8;
-    const uint32_t g0 = ctl.gen_wait[b & 1];
+    const uint32_t* cnt = a.sync + (int64_t)r * 16;
     const uint64_t start = global_timer_ns();
-    while (ld_acquire_gpu(gen) == g0) {
+    while (ld_acquire_gpu(cnt) < (uint32_t)G) {
       if (global_timer_ns() - start > ctl.timeout_ns) {
         ctl.abort = 1;
         atomicOr(a.status, T2VA_STATUS_TIMEOUT);
@@ -300,159 +391,141 @@ __device__ bool wait_and_merge(const ObjectiveArgs& a, SmemCtl& ctl, int b, int 
   }
   __syncthreads();
   if (ctl.abort) return false;
-  if (warp < a.M * kQuantities) {
-    const int m = warp / kQuantities, q = warp - m * kQuantities;
-    const float* src = a.partials + ((int64_t)(b * a.M + m) * kQuantities + q) * a.gmax;
+  const int per_bl = a.M * kQuantities;
+  const float qnan = __int_as_float(0x7fc00000);
+  for (int u = warp; u < nb * per_bl; u += kWarps) {
+    const int bl = u / per_bl;
+    const int m = (u - bl * per_bl) / kQuantities;
+    const int q = u - bl * per_bl - m * kQuantities;
+    const float* src = a.partials + (((int64_t)(b0 + bl) * a.M + m) * kQuantities + q) * a.gmax;
     float s = 0.f;
     for (int i = lane; i < G; i += 32) s += __ldcg(src + i);
     s = warp_sum(s);
-    if (lane == 0) ctl.tot[m][q] = s;
+    if (lane == 0) {
+      ctl.tot[gi][bl][m][q] = s;
+      const RoundCoef& k = ctl.coef[gi][bl];
+      if (Tr::kScm && q == 0) {
+        const float n = sqrtf(s);
+        ctl.scaleS[gi][bl][m] = 2.f * a.lam_s * a.w[m] / (k.s * (n + a.eps_s));
+      }
+      if (Tr::kDmd && q == 1) {
+        const float c = a.n[m] > 0 ? s / (float)a.n[m] : 0.f;
+        ctl.scaleD[gi][bl][m] = k.ok ? 2.f * a.lam_d * a.w[m] / (c + a.eps_d) : qnan;
+      }
+    }
   }
   __syncthreads();
   return true;
 }
 
+__device__ __forceinline__ void write4(float* dst, float4 o, int accumulate) {
+  float4* d = reinterpret_cast<float4*>(dst);
+  if (accumulate) {
+    const float4 old = *d;
+    o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+  }
+  st_stream16(d, o);
+}
+
 template <typename T, int MODE>
-__device__ void phase_w(const ObjectiveArgs& a, SmemCtl& ctl, const float4* slot, int b, int cta,
+__device__ __forceinline__ void write_vec(const ObjectiveArgs& a, int m, int64_t e, float scS,
+                                          float scD, const float* gs, const float* gd) {
+  using Tr = Traits<T, MODE>;
+  constexpr int VE = Tr::VE;
+  const bool alias = Tr::kScm && Tr::kDmd && ((a.alias_mask >> m) & 1u);
+#pragma unroll
+  for (int i = 0; i < VE; i += 4) {
+    if (alias) {
+      write4(a.grad_s[m] + e + i,
+             make_float4(scS * gs[i] + scD * gd[i], scS * gs[i + 1] + scD * gd[i + 1],
+                         scS * gs[i + 2] + scD * gd[i + 2], scS * gs[i + 3] + scD * gd[i + 3]),
+             a.accumulate);
+    } else {
+      if constexpr (Tr::kScm)
+        write4(a.grad_s[m] + e + i,
+               make_float4(scS * gs[i], scS * gs[i + 1], scS * gs[i + 2], scS * gs[i + 3]),
+               a.accumulate);
+      if constexpr (Tr::kDmd)
+        write4(a.grad_d[m] + e + i,
+               make_float4(scD * gd[i], scD * gd[i + 1], scD * gd[i + 2], scD * gd[i + 3]),
+               a.accumulate);
+    }
+  }
+}
+
+__device__ __forceinline__ void write1(float* dst, float v, int accumulate) {
+  if (accumulate) v += *dst;
+  *dst = v;
+}
+
+template <typename T, int MODE>
+__device__ void phase_w(const ObjectiveArgs& a, SmemCtl& ctl, const float4* group, int r, int cta,
                         int G) {
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t V = sample_vectors<VE>(a, b);
-  const int64_t lo = V * cta / G, hi = V * (cta + 1) / G;
-  const Coef k = Tr::kScm ? sample_coef(__ldg(a.t + b), a.beta, a.gamma) : Coef{0, 0, 0, 0, 0, true};
+  const int tid = threadIdx.x;
+  const int gi = r % a.groups;
+  const int b0 = r * a.spr;
+  const int nb = min(a.spr, a.B - b0);
   const float qnan = __int_as_float(0x7fc00000);
 
-  int64_t voff = 0;
-  for (int m = 0; m < a.M; ++m) {
-    const SegGeom g = seg_geom<VE>(a.n[m], a.stride[m], b);
-    // per-(sample, modality) gradient factors
-    float scS = 0.f, scD = 0.f;
-    if constexpr (Tr::kScm) {
-      const float n = sqrtf(ctl.tot[m][0]);
-      scS = 2.f * a.lam_s * a.w[m] / (k.s * (n + a.eps_s));
-    }
-    if constexpr (Tr::kDmd) {
-      const float c = a.n[m] > 0 ? ctl.tot[m][1] / (float)a.n[m] : 0.f;
-      scD = 2.f * a.lam_d * a.w[m] / (c + a.eps_d);
-      if (!k.ok) scD = qnan;
-    }
-    const bool alias = Tr::kScm && Tr::kDmd && ((a.alias_mask >> m) & 1u);
-    float* outS = a.grad_s[m];
-    float* outD = a.grad_d[m];
-    const int64_t a0 = max(lo, voff), a1 = min(hi, voff + g.nvec);
-    const int64_t ebase = g.e0 + g.head - voff * VE;
-    voff += g.nvec;
-    for (int64_t v = a0 + tid; v < a1; v += kThreads * kUnroll) {
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int64_t vv = v + u * kThreads;
-        if (vv < a1) {
-          const int64_t pos = vv - lo;
-          const int64_t e = ebase + vv * VE;
-          float gs[VE], gd[VE];
-          if (pos < a.cap) {
-            const float4* src = slot + pos;
-            int p = 0;
-            if constexpr (Tr::kScm) {
-#pragma unroll
-              for (int i = 0; i < VE; i += 4, ++p) {
-                const float4 f = src[(int64_t)p * a.cap];
-                gs[i] = f.x; gs[i + 1] = f.y; gs[i + 2] = f.z; gs[i + 3] = f.w;
-              }
-            }
-            if constexpr (Tr::kDmd) {
-#pragma unroll
-              for (int i = 0; i < VE; i += 4, ++p) {
-                const float4 f = src[(int64_t)p * a.cap];
-                gd[i] = f.x; gd[i + 1] = f.y; gd[i + 2] = f.z; gd[i + 3] = f.w;
-              }
-            }
-          } else {
-            Loaded<T, MODE> L;
-            load_vec<T, MODE>(L, a, m, e);
-            float d0 = 0.f, d1 = 0.f, d2 = 0.f;
-            directions<T, MODE>(L, k, gs, gd, d0, d1, d2);
-          }
-#pragma unroll
-          for (int i = 0; i < VE; i += 4) {
-            if (alias) {
-              float4 o = make_float4(scS * gs[i] + scD * gd[i], scS * gs[i + 1] + scD * gd[i + 1],
-                                     scS * gs[i + 2] + scD * gd[i + 2],
-                                     scS * gs[i + 3] + scD * gd[i + 3]);
-              float4* dst = reinterpret_cast<float4*>(outS + e + i);
-              if (a.accumulate) {
-                const float4 old = *dst;
-                o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
-              }
-              st_stream16(dst, o);
-            } else {
-              if constexpr (Tr::kScm) {
-                float4 o = make_float4(scS * gs[i], scS * gs[i + 1], scS * gs[i + 2], scS * gs[i + 3]);
-                float4* dst = reinterpret_cast<float4*>(outS + e + i);
-                if (a.accumulate) {
-                  const float4 old = *dst;
-                  o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
-                }
-                st_stream16(dst, o);
-              }
-              if constexpr (Tr::kDmd) {
-                float4 o = make_float4(scD * gd[i], scD * gd[i + 1], scD * gd[i + 2], scD * gd[i + 3]);
-                float4* dst = reinterpret_cast<float4*>(outD + e + i);
-                if (a.accumulate) {
-                  const float4 old = *dst;
-                  o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
-                }
-                st_stream16(dst, o);
-              }
-            }
-          }
-        }
+  Item it;
+  bool more = first_item(it, nb, a);
+  while (more) {
+    const ItemInfo ic = item_info<VE>(it, b0, cta, a);
+    if (ic.valid) {
+      float gs[VE], gd[VE];
+      if (ic.pos < a.cap[it.m]) {
+        fetch<T, MODE>(group + it.bl * a.sample_f4 + a.choff[it.m], a.cap[it.m], ic.pos, gs, gd);
+      } else {  // not kept on chip: recompute from the inputs
+        Loaded<T, MODE> L;
+        load_vec<T, MODE>(L, a, it.m, ic.e);
+        float d0 = 0.f, d1 = 0.f, d2 = 0.f;
+        directions<T, MODE>(L, ctl.coef[gi][it.bl], gs, gd, d0, d1, d2);
       }
+      const float scS = Tr::kScm ? ctl.scaleS[gi][it.bl][it.m] : 0.f;
+      const float scD = Tr::kDmd ? ctl.scaleD[gi][it.bl][it.m] : 0.f;
+      write_vec<T, MODE>(a, it.m, ic.e, scS, scD, gs, gd);
     }
-    // unaligned head/tail elements
-    if (warp == 0 && cta == scalar_owner(b, m, a.M, G)) {
-      int64_t e = -1;
-      if (lane < g.head) e = g.e0 + lane;
-      else if (lane >= 8 && lane - 8 < g.tail) e = g.e0 + g.head + g.nvec * VE + (lane - 8);
-      if (e >= 0) {
-        float gs = 0.f, gd = 0.f;
-        direction_scalar<T, MODE>(a, m, e, k, gs, gd);
-        if (alias) {
-          float o = scS * gs + scD * gd;
-          if (a.accumulate) o += outS[e];
-          outS[e] = o;
-        } else {
-          if constexpr (Tr::kScm) {
-            float o = scS * gs;
-            if (a.accumulate) o += outS[e];
-            outS[e] = o;
-          }
-          if constexpr (Tr::kDmd) {
-            float o = scD * gd;
-            if (a.accumulate) o += outD[e];
-            outD[e] = o;
-          }
-        }
+    more = next_item(it, nb, a);
+  }
+
+  // unaligned head/tail elements (CTA G-1)
+  if (cta == G - 1) {
+    int bl, m;
+    const int64_t e = scalar_element<VE>(a, b0, nb, bl, m);
+    if (e >= 0) {
+      float gs = 0.f, gd = 0.f, sabs = 0.f;
+      scalar_direction<T, MODE>(a, m, e, ctl.coef[gi][bl], gs, gd, sabs);
+      const float scS = Tr::kScm ? ctl.scaleS[gi][bl][m] : 0.f;
+      const float scD = Tr::kDmd ? ctl.scaleD[gi][bl][m] : 0.f;
+      if (Tr::kScm && Tr::kDmd && ((a.alias_mask >> m) & 1u)) {
+        write1(a.grad_s[m] + e, scS * gs + scD * gd, a.accumulate);
+      } else {
+        if constexpr (Tr::kScm) write1(a.grad_s[m] + e, scS * gs, a.accumulate);
+        if constexpr (Tr::kDmd) write1(a.grad_d[m] + e, scD * gd, a.accumulate);
       }
     }
   }
 
-  // per-sample outputs, written by one CTA
-  if (tid == 0 && cta == (int)(b % G)) {
+  // per-sample outputs: sample b is written by CTA b % G
+  for (int bl = tid; bl < nb; bl += kThreads) {
+    const int b = b0 + bl;
+    if (b % G != cta) continue;
+    const RoundCoef& k = ctl.coef[gi][bl];
     float Ls = 0.f, Ld = 0.f;
     for (int m = 0; m < a.M; ++m) {
       if constexpr (Tr::kScm) {
-        const float Sg = ctl.tot[m][0];
+        const float Sg = ctl.tot[gi][bl][m][0];
         const float n = sqrtf(Sg);
         const float d = n + a.eps_s;
         Ls += a.w[m] * (Sg / (d * d));
         if (a.norm) a.norm[(int64_t)b * a.M + m] = k.ok ? n : qnan;
       }
       if constexpr (Tr::kDmd) {
-        const float c = a.n[m] > 0 ? ctl.tot[m][1] / (float)a.n[m] : 0.f;
+        const float c = a.n[m] > 0 ? ctl.tot[gi][bl][m][1] / (float)a.n[m] : 0.f;
         const float d = c + a.eps_d;
-        Ld += a.w[m] * (ctl.tot[m][2] / (d * d));
+        Ld += a.w[m] * (ctl.tot[gi][bl][m][2] / (d * d));
         if (a.cdmd) a.cdmd[(int64_t)b * a.M + m] = k.ok ? c : qnan;
       }
     }
@@ -473,9 +546,8 @@ template <typename T, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) k_objective(const __grid_constant__ ObjectiveArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(smem_raw);
-  float4* slots = reinterpret_cast<float4*>(smem_raw + kCtlBytes);
-  using Tr = Traits<T, MODE>;
-  const int64_t slot_f4 = (int64_t)a.cap * Tr::P;
+  float4* groups = reinterpret_cast<float4*>(smem_raw + kCtlBytes);
+  const int64_t group_f4 = (int64_t)a.spr * a.sample_f4;
   const int G = gridDim.x, cta = blockIdx.x;
   if (threadIdx.x == 0) {
     ctl.abort = 0;
@@ -483,20 +555,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_objective(const __grid_constant
   }
   __syncthreads();
 
-  const int K = a.slots;
-  for (int b = 0; b < a.B; ++b) {
-    if (b >= K) __syncthreads();  // slot (b % K) was last read in W(b - K) by other threads
-    phase_a<T, MODE>(a, ctl, slots + (b % K) * slot_f4, b, cta, G);
-    const int wb = (K == 1) ? b : b - 1;
-    if (wb >= 0) {
-      if (!wait_and_merge<MODE>(a, ctl, wb, G)) return;
-      phase_w<T, MODE>(a, ctl, slots + (wb % K) * slot_f4, wb, cta, G);
+  const int K = a.groups;
+  for (int r = 0; r < a.rounds; ++r) {
+    phase_a<T, MODE>(a, ctl, groups + (r % K) * group_f4, r, cta, G);
+    const int wr = (K == 1) ? r : r - 1;
+    if (wr >= 0) {
+      if (!wait_and_merge<T, MODE>(a, ctl, wr, G)) return;
+      phase_w<T, MODE>(a, ctl, groups + (wr % K) * group_f4, wr, cta, G);
     }
   }
-  if (K > 1 && a.B > 0) {
-    const int wb = a.B - 1;
-    if (!wait_and_merge<MODE>(a, ctl, wb, G)) return;
-    phase_w<T, MODE>(a, ctl, slots + (wb % K) * slot_f4, wb, cta, G);
+  if (K > 1 && a.rounds > 0) {
+    const int wr = a.rounds - 1;
+    if (!wait_and_merge<T, MODE>(a, ctl, wr, G)) return;
+    phase_w<T, MODE>(a, ctl, groups + (wr % K) * group_f4, wr, cta, G);
+  }
+  // The last CTA to get here resets the round counters for the next call: every
+  // other CTA finished all of its waits before counting itself out.
+  if (threadIdx.x == 0) {
+    const uint32_t old = atomicAdd(&a.hdr->exit_count, 1u);
+    if (old == (uint32_t)(G - 1)) {
+      for (int r = 0; r < a.rounds; ++r) a.sync[(int64_t)r * 16] = 0u;
+      a.hdr->exit_count = 0u;
+    }
   }
 }
 
@@ -511,7 +591,7 @@ cudaError_t launch_t(const ObjectiveArgs& a, const ObjectiveLaunch& l, cudaStrea
   cfg.dynamicSmemBytes = l.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].id = cudaLaunchAttributeCooperative;  // every CTA is resident: the waits always end
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -524,11 +604,12 @@ __global__ void k_ws_init(uint4* ws, size_t n16, uint64_t timeout_ns, uint32_t g
     ws[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   if (blockIdx.x == 0 && threadIdx.x == 0) {
-    // block 0 also zeroed the header words above; write them after its own barrier
+    // block 0 zeroed the header above; write its fields after that block's barrier
     WsHeader* h = reinterpret_cast<WsHeader*>(ws);
     h->timeout_ns = timeout_ns;
     h->gmax = gmax;
     h->poisoned = 0;
+    h->exit_count = 0;
     __threadfence();
     h->magic = kWsMagic;
   }
@@ -540,30 +621,50 @@ bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int mode, int sm_count, siz
                     ObjectiveLaunch* out) {
   const int VE = dt == T2VA_BFLOAT16 ? 8 : 4;
   const int Q = ((mode & kModeScm) ? 1 : 0) + ((mode & kModeDmd) ? 1 : 0);
-  const int P = Q * VE / 4;
-  int64_t vmax = 0;
-  for (int m = 0; m < a.M; ++m) vmax += (a.n[m] + VE - 1) / VE;
-  int64_t G = (vmax + kThreads - 1) / kThreads;
-  if (G < 1) G = 1;
-  if (G > sm_count) G = sm_count;
-  if (G > a.gmax) G = a.gmax;
-  const int64_t per_cta = (vmax + G - 1) / G;
-  const size_t bytes_per_vec = (size_t)P * 16;
-  if (smem_optin <= kCtlBytes + bytes_per_vec) return false;
-  const size_t budget = smem_optin - kCtlBytes;
-  int slots = 1;
-  int64_t cap = per_cta;
-  if (a.B >= 2 && (size_t)(2 * per_cta) * bytes_per_vec <= budget) {
-    slots = 2;
-  } else if ((size_t)per_cta * bytes_per_vec > budget) {
-    cap = (int64_t)(budget / bytes_per_vec);
+  const int64_t P = (int64_t)Q * VE / 4;  // float4 pieces kept per vector
+  int64_t vtot = 0, nvec_ub[kMaxM];
+  for (int m = 0; m < a.M; ++m) {
+    nvec_ub[m] = (a.n[m] + VE - 1) / VE;
+    vtot += nvec_ub[m];
   }
-  if (cap < 1) cap = 1;
-  a.slots = slots;
-  a.cap = (int)cap;
+  int64_t G = (vtot + kThreads - 1) / kThreads;  // small problems use fewer CTAs
+  G = std::max<int64_t>(1, std::min<int64_t>({G, (int64_t)sm_count, (int64_t)a.gmax}));
+  int64_t per_sample_f4 = 0;
+  for (int m = 0; m < a.M; ++m) {
+    a.chunk[m] = (nvec_ub[m] + G - 1) / G;
+    const int64_t it = (a.chunk[m] + kThreads - 1) / kThreads;
+    if (it > INT32_MAX) return false;
+    a.iters[m] = (int)it;
+    per_sample_f4 += P * a.chunk[m];
+  }
+  if (smem_optin <= kCtlBytes + 16 * (size_t)P) return false;
+  const int64_t budget_f4 = (int64_t)((smem_optin - kCtlBytes) / 16);
+  int64_t keep_num = 1, keep_den = 1;  // fraction of each chunk kept on chip
+  if (a.B >= 2 && 2 * per_sample_f4 <= budget_f4) {
+    a.groups = 2;
+    const int64_t spr = std::min<int64_t>(budget_f4 / (2 * per_sample_f4), (a.B + 1) / 2);
+    a.spr = (int)std::max<int64_t>(1, std::min<int64_t>(spr, kMaxRound));
+  } else if (per_sample_f4 <= budget_f4) {
+    a.groups = 1;
+    const int64_t spr = per_sample_f4 > 0 ? std::min<int64_t>(budget_f4 / per_sample_f4, a.B) : a.B;
+    a.spr = (int)std::max<int64_t>(1, std::min<int64_t>(spr, kMaxRound));
+  } else {
+    a.groups = 1;
+    a.spr = 1;
+    keep_num = budget_f4;
+    keep_den = per_sample_f4;
+  }
+  int64_t off = 0;
+  for (int m = 0; m < a.M; ++m) {
+    a.cap[m] = a.chunk[m] * keep_num / keep_den;
+    a.choff[m] = off;
+    off += P * a.cap[m];
+  }
+  a.sample_f4 = off;
+  a.rounds = (a.B + a.spr - 1) / a.spr;
   out->grid = (int)G;
   out->threads = kThreads;
-  out->smem = kCtlBytes + (size_t)slots * cap * bytes_per_vec;
+  out->smem = kCtlBytes + (size_t)a.groups * a.spr * a.sample_f4 * 16;
   return true;
 }
 
@@ -582,9 +683,7 @@ cudaError_t launch_objective(const ObjectiveArgs& a, t2va_dtype dt, int mode,
 cudaError_t launch_workspace_init(void* ws, size_t bytes, uint64_t timeout_ns, uint32_t gmax,
                                   cudaStream_t st) {
   const size_t n16 = bytes / 16;
-  int blocks = (int)((n16 + 255) / 256);
-  if (blocks > 1024) blocks = 1024;
-  if (blocks < 1) blocks = 1;
+  int blocks = (int)std::min<size_t>(1024, std::max<size_t>(1, (n16 + 255) / 256));
   k_ws_init<<<blocks, 256, 0, st>>>(reinterpret_cast<uint4*>(ws), n16, timeout_ns, gmax);
   return cudaGetLastError();
 }
