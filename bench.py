@@ -112,6 +112,30 @@ def committed_traffic(workload: str):
 
 
 # ---------------------------------------------------------------------------
+# multi-rank host logic (one process per GPU; samples are sharded by rank)
+# ---------------------------------------------------------------------------
+
+def rank_seed_offset(rank: int, input_set: int) -> int:
+    """Seed key suffix of input set `input_set` on `rank`: every rank draws its own samples."""
+    return 1000 * rank + input_set
+
+
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The slowest rank's time: the whole job ends when its last rank ends."""
+    if dist is None:
+        return float(ms)
+    import torch
+    tt = torch.tensor([float(ms)], device=device, dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_gbs(world: int, bytes_per_step_per_rank: int, steps: int, ms: float) -> float:
+    """Algorithmic bytes of all ranks' steps over the (max-over-ranks) time, in GB/s."""
+    return world * bytes_per_step_per_rank * steps / (ms * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 
@@ -252,7 +276,7 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     sets = []
     host0 = None
     for r in range(R):
-        inp = S.make_workload_inputs(wl, seed_offset=1000 * rank + r)
+        inp = S.make_workload_inputs(wl, seed_offset=rank_seed_offset(rank, r))
         if r == 0:
             host0 = inp
         d = {f: [to_dev(a) for a in getattr(inp, f)] for f in fields_in}
@@ -369,14 +393,9 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     if st != 0:
         raise RuntimeError(f"device status {st} during the benchmark")
 
-    if dist is not None:
-        import torch.distributed as tdist
-        tt = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
-
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
     ms_per_step = elapsed_ms / K
-    value = world * nb["step"] * K / (elapsed_ms * 1e-3) / 1e9
+    value = whole_job_gbs(world, nb["step"], K, elapsed_ms)
     obj_mean_ms = float(np.mean(obj_ms))
     obj_gbs = nb["objective"] / (obj_mean_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
@@ -467,14 +486,9 @@ def run_e2e(args, wl, host0, d0, ws, status, noise, objective, dev, nb, world, d
         one()
     e1.record(stream)
     stream.synchronize()
-    ms = e0.elapsed_time(e1)
-    if dist is not None:
-        import torch.distributed as tdist
-        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     assert int(status.item()) == 0
-    return {"value": round(world * nb["step"] * steps / (ms * 1e-3) / 1e9, 3), "unit": UNIT,
+    return {"value": round(whole_job_gbs(world, nb["step"], steps, ms), 3), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": ms / steps}
 

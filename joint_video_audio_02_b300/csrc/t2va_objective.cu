@@ -379,7 +379,8 @@ __device__ bool wait_and_merge(const ObjectiveArgs& a, SmemCtl& ctl, int r, int 
   if (tid == 0 && !ctl.abort) {
     const uint32_t* cnt = a.sync + (int64_t)r * 16;
     const uint64_t start = global_timer_ns();
-    while (ld_acquire_gpu(cnt) < (uint32_t)G) {
+    // signed: a counter that holds a negative value never reaches G (the timeout test's planted state)
+    while ((int32_t)ld_acquire_gpu(cnt) < G) {
       if (global_timer_ns() - start > ctl.timeout_ns) {
         ctl.abort = 1;
         atomicOr(a.status, T2VA_STATUS_TIMEOUT);

@@ -300,7 +300,7 @@ def test_timeout_sets_status_and_poisons_workspace():
     p = Params()
     ws = t2va.new_workspace(2, 2, timeout_ms=200)
     torch.cuda.synchronize()
-    ws.view(torch.int32)[64] = 0x40000000   # sample 0's arrival counter
+    ws.view(torch.int32)[64] = -(1 << 30)   # round 0's arrival counter: G arrivals never reach G
     bad = gpu_run(inp, p, S.STAGE3, workspace=ws)
     assert bad["status"] & t2va.STATUS_TIMEOUT
     again = gpu_run(inp, p, S.STAGE3, workspace=ws)
