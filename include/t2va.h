@@ -189,6 +189,55 @@ int t2va_stage3_objective(int batch, int num_modalities, const t2va_segment* seg
                           void* workspace, size_t workspace_bytes, int* status,
                           cudaStream_t stream);
 
+/* Bytes of the library's own scratch array used by
+ * t2va_stage3_objective_noalloc (1 MiB). Every GPU that loads the library holds
+ * this much device memory until the process exits. */
+#define T2VA_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* The stage-3 objective without a caller-provided workspace.
+ *
+ * The paper has no counterpart: this entry point is for callers that cannot
+ * allocate device memory. Examples are code that runs inside another runtime's
+ * memory pool or under an allocator that owns all device memory, plugins that
+ * get only their inputs and outputs from a host, and hosts that forbid
+ * allocation after set-up. Such callers cannot provide the workspace that
+ * t2va_stage3_objective needs.
+ *
+ * The arguments, outputs and results are those of t2va_stage3_objective,
+ * without `workspace` and `workspace_bytes`. In their place the call uses a
+ * scratch array owned by the library: T2VA_NOALLOC_SCRATCH_BYTES of static
+ * device memory per GPU. The call allocates nothing: no cudaMalloc, no cudaFree
+ * and no allocating library routine.
+ *
+ * - Limit: the workspace that `batch` and `num_modalities` need on the current
+ *   device (t2va_workspace_bytes) must fit in the scratch. About 290 samples of
+ *   2 modalities fit on a 148-SM GPU. A larger batch returns
+ *   T2VA_ERROR_WORKSPACE, and nothing is enqueued.
+ * - First call: the first call on each device, with that device current, looks
+ *   up the scratch's device address (cudaGetSymbolAddress) and keeps it. Make
+ *   that first call before any stream capture on that device.
+ * - Sharing: every call on a device shares the one scratch array, which keeps
+ *   what the last call left there. Each call first re-initialises the array's
+ *   header and arrival counters with one small kernel on `stream`, then
+ *   launches the objective. Calls that overlap on the GPU (on different streams
+ *   or from different host threads) race on the array and give wrong results.
+ *   Order them on one stream, or use t2va_stage3_objective with one workspace
+ *   per concurrent call.
+ * - Errors: argument errors are those of t2va_stage3_objective, returned before
+ *   anything is enqueued. T2VA_ERROR_CUDA means the scratch's address could not
+ *   be obtained. */
+int t2va_stage3_objective_noalloc(int batch, int num_modalities, const t2va_segment* seg,
+                                  t2va_dtype dtype, const void* const* z_t,
+                                  const void* const* x0_teacher, const void* const* x0_student,
+                                  const void* const* x0_student_tangent, const float* t,
+                                  const void* const* zhat0, const void* const* x0_teacher_hat,
+                                  const void* const* x0_fake, float beta, float gamma,
+                                  float eps_scm, float eps_dmd, const float* weight,
+                                  float lambda_scm, float lambda_dmd,
+                                  float* const* grad_x0_student, float* const* grad_zhat0,
+                                  int accumulate, float* loss, float* loss_scm, float* loss_dmd,
+                                  float* norm, float* cdmd, int* status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     noise,
     scm_objective,
     stage3_objective,
+    stage3_objective_noalloc,
     workspace_bytes,
     workspace_init,
 )

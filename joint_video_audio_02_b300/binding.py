@@ -31,8 +31,11 @@ STATUS_BAD_TIMESTEP = 0x1
 STATUS_TIMEOUT = 0x2
 STATUS_BAD_WORKSPACE = 0x4
 
+NOALLOC_SCRATCH_BYTES = 1 << 20   # T2VA_NOALLOC_SCRATCH_BYTES
+
 EXPORTED = ("t2va_error_string", "t2va_abi_version", "t2va_workspace_bytes", "t2va_workspace_init",
-            "t2va_noise", "t2va_scm_objective", "t2va_dmd_objective", "t2va_stage3_objective")
+            "t2va_noise", "t2va_scm_objective", "t2va_dmd_objective", "t2va_stage3_objective",
+            "t2va_stage3_objective_noalloc")
 
 
 class Segment(ctypes.Structure):
@@ -72,6 +75,10 @@ def _declare(lib):
                                           c_float, c_float, c_float, c_float, P, c_float, c_float,
                                           P, P, c_int, P, P, P, P, P, P, c_size_t, P, P]
     lib.t2va_stage3_objective.restype = c_int
+    lib.t2va_stage3_objective_noalloc.argtypes = [c_int, c_int, seg, c_int, P, P, P, P, P, P, P, P,
+                                                  c_float, c_float, c_float, c_float, P, c_float,
+                                                  c_float, P, P, c_int, P, P, P, P, P, P, P]
+    lib.t2va_stage3_objective_noalloc.restype = c_int
 
 
 def load(path: Optional[str] = None):
@@ -233,3 +240,28 @@ def stage3_objective(z_t, x0_teacher, x0_student, x0_student_tangent, t, zhat0, 
         loss.data_ptr(), _opt(loss_scm), _opt(loss_dmd), _opt(norm), _opt(cdmd),
         workspace.data_ptr(), workspace.numel() * workspace.element_size(), status.data_ptr(),
         _stream(stream)), "t2va_stage3_objective")
+
+
+def stage3_objective_noalloc(z_t, x0_teacher, x0_student, x0_student_tangent, t, zhat0,
+                             x0_teacher_hat, x0_fake, *, beta, gamma, eps_scm, eps_dmd, weight,
+                             lambda_scm, lambda_dmd, grad_x0_student, grad_zhat0, loss,
+                             loss_scm=None, loss_dmd=None, norm=None, cdmd=None, accumulate=False,
+                             status, stream=None):
+    """stage3_objective for callers that cannot allocate device memory: no workspace
+    argument; the library's own static scratch array is used instead (one per GPU,
+    shared by every call, so calls that overlap on the GPU race). The first call on a
+    device looks up the array's address and should come before any stream capture."""
+    B, M = int(t.shape[0]), len(z_t)
+    segs = _segments([z_t, x0_teacher, x0_student, x0_student_tangent, zhat0, x0_teacher_hat,
+                      x0_fake, grad_x0_student, grad_zhat0], B)
+    dt = _dtype_code(z_t[0].dtype)
+    for g in list(grad_x0_student) + list(grad_zhat0):
+        _f32(g, "gradient")
+    w = (c_float * M)(*[float(x) for x in weight])
+    _check(load().t2va_stage3_objective_noalloc(
+        B, M, segs, dt, _ptrs(z_t), _ptrs(x0_teacher), _ptrs(x0_student), _ptrs(x0_student_tangent),
+        t.data_ptr(), _ptrs(zhat0), _ptrs(x0_teacher_hat), _ptrs(x0_fake),
+        float(beta), float(gamma), float(eps_scm), float(eps_dmd), w, float(lambda_scm),
+        float(lambda_dmd), _ptrs(grad_x0_student), _ptrs(grad_zhat0), int(bool(accumulate)),
+        loss.data_ptr(), _opt(loss_scm), _opt(loss_dmd), _opt(norm), _opt(cdmd),
+        status.data_ptr(), _stream(stream)), "t2va_stage3_objective_noalloc")

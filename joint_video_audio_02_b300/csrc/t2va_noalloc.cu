@@ -1,0 +1,93 @@
+// Allocation-free variant of the stage-3 objective entry point.
+//
+// Some callers cannot call cudaMalloc, or any routine that allocates: code that
+// runs inside another runtime's memory pool or under a custom allocator that
+// owns all device memory, plugins that get only the inputs and outputs from
+// their host, and hosts that forbid allocation once set-up is over. They cannot
+// provide the caller-owned workspace that t2va_stage3_objective needs. This
+// entry point uses instead a scratch array of fixed size that belongs to the
+// library: a file-scope __device__ array, held by every GPU that loads the
+// library until the process exits. The caller still passes every input and
+// output buffer.
+//
+// Host code cannot use the array's name as a device address: on the host it
+// names a host-side stand-in. So the first call on each device, with that
+// device current, asks the runtime for the array's device address
+// (cudaGetSymbolAddress) and keeps it; later calls on that device reuse it.
+#include <mutex>
+
+#include "t2va_internal.cuh"
+
+using namespace t2va;
+
+namespace {
+
+static_assert(T2VA_NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size");
+
+// The scratch array. Every call on a device shares it.
+static __device__ __align__(256) unsigned char g_scratch[T2VA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_dev[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+// Device address of g_scratch on the current device, looked up once per device.
+int scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return T2VA_ERROR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_dev[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return T2VA_ERROR_CUDA;
+    }
+    g_scratch_dev[dev] = p;
+  }
+  *out = g_scratch_dev[dev];
+  return T2VA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" int t2va_stage3_objective_noalloc(
+    int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+    const void* const* z_t, const void* const* x0_teacher, const void* const* x0_student,
+    const void* const* x0_student_tangent, const float* t, const void* const* zhat0,
+    const void* const* x0_teacher_hat, const void* const* x0_fake, float beta, float gamma,
+    float eps_scm, float eps_dmd, const float* weight, float lambda_scm, float lambda_dmd,
+    float* const* grad_x0_student, float* const* grad_zhat0, int accumulate, float* loss,
+    float* loss_scm, float* loss_dmd, float* norm, float* cdmd, int* status,
+    cudaStream_t stream) {
+  // Every argument check of t2va_stage3_objective comes before its workspace
+  // check, so a call without a workspace returns T2VA_ERROR_WORKSPACE exactly when
+  // everything else is valid, and enqueues nothing. An empty batch returns success.
+  const int pre = t2va_stage3_objective(
+      batch, num_modalities, seg, dtype, z_t, x0_teacher, x0_student, x0_student_tangent, t,
+      zhat0, x0_teacher_hat, x0_fake, beta, gamma, eps_scm, eps_dmd, weight, lambda_scm,
+      lambda_dmd, grad_x0_student, grad_zhat0, accumulate, loss, loss_scm, loss_dmd, norm, cdmd,
+      nullptr, 0, status, stream);
+  if (pre != T2VA_ERROR_WORKSPACE) return pre;
+  // the scratch must hold the workspace this batch needs on this device
+  const size_t need = t2va_workspace_bytes(batch, num_modalities);
+  if (need == 0) return T2VA_ERROR_CUDA;
+  if (need > (size_t)T2VA_NOALLOC_SCRATCH_BYTES) return T2VA_ERROR_WORKSPACE;
+  void* ws = nullptr;
+  const int rc = scratch_address(&ws);
+  if (rc != T2VA_SUCCESS) return rc;
+  // The array keeps whatever the last call left there. Re-initialise its header
+  // and arrival counters (they must start at zero; a timed-out call also leaves
+  // the poisoned flag set). The partial sums need no clearing: every slot is
+  // written before it is read. This is one small kernel on `stream`.
+  const size_t counters = ws_partials_offset(batch);
+  const int init = t2va_workspace_init(ws, counters, 0, stream);
+  if (init != T2VA_SUCCESS) return init;
+  return t2va_stage3_objective(batch, num_modalities, seg, dtype, z_t, x0_teacher, x0_student,
+                               x0_student_tangent, t, zhat0, x0_teacher_hat, x0_fake, beta, gamma,
+                               eps_scm, eps_dmd, weight, lambda_scm, lambda_dmd, grad_x0_student,
+                               grad_zhat0, accumulate, loss, loss_scm, loss_dmd, norm, cdmd, ws,
+                               (size_t)T2VA_NOALLOC_SCRATCH_BYTES, status, stream);
+}

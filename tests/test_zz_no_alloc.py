@@ -1,0 +1,96 @@
+"""The allocation-free stage-3 entry point against the regular one.
+
+t2va_stage3_objective_noalloc serves callers that cannot allocate device memory
+(code running inside another runtime's memory pool or under an allocator that owns
+all device memory, plugins handed only their inputs and outputs, hosts that forbid
+allocation after set-up): it takes no workspace and uses the library's static
+scratch array instead. Its results must match t2va_stage3_objective's on the same
+inputs within the parity tolerances, on two calls in a row (the second call finds
+the scratch as the first one left it).
+
+This file is collected last, so a run that stops at the first failure has run
+every other test before it. It must also pass alone in a fresh process.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import joint_video_audio_02_b300 as t2va
+import synthetic as S
+from joint_video_audio_02_b300.build import build
+from t2va_gpu_util import GRAD_FRAC, RTOL, Params, grads_like, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build()
+    t2va.load()
+
+
+def _run(inp, p, noalloc):
+    dt = inp.dtype
+    B, M = inp.batch, len(inp.z0)
+    t = torch.from_numpy(inp.t).cuda()
+    zt = to_device(inp.z0, dt)               # the objective's z_t input (noising is not under test)
+    xT, xS, tan = (to_device(getattr(inp, f), dt) for f in ("x0_teacher", "x0_student", "x0_tangent"))
+    zh, yT, yF = (to_device(getattr(inp, f), dt) for f in ("zhat0", "x0_teacher_hat", "x0_fake"))
+    gS, gD = grads_like(zt, float("nan")), grads_like(zh, float("nan"))
+    loss = torch.full((B,), float("nan"), device="cuda")
+    norm = torch.full((B * M,), float("nan"), device="cuda")
+    cdmd = torch.full((B * M,), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kw = dict(beta=p.beta, gamma=p.gamma, eps_scm=p.eps_scm, eps_dmd=p.eps_dmd, weight=p.weight,
+              lambda_scm=p.lambda_scm, lambda_dmd=p.lambda_dmd, grad_x0_student=gS, grad_zhat0=gD,
+              loss=loss, norm=norm, cdmd=cdmd, status=status)
+    if noalloc:
+        t2va.stage3_objective_noalloc(zt, xT, xS, tan, t, zh, yT, yF, **kw)
+    else:
+        ws = t2va.new_workspace(B, M)
+        t2va.stage3_objective(zt, xT, xS, tan, t, zh, yT, yF, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    return {"status": int(status.item()), "loss": loss.cpu().numpy(), "norm": norm.cpu().numpy(),
+            "cdmd": cdmd.cpu().numpy(), "gS": [g.cpu().numpy() for g in gS],
+            "gD": [g.cpu().numpy() for g in gD]}
+
+
+def _same(got, ref, dtype):
+    assert got["status"] == 0 and ref["status"] == 0
+    rtol = RTOL[dtype]
+    for k in ("loss", "norm", "cdmd"):
+        np.testing.assert_allclose(got[k], ref[k], rtol=rtol, atol=0)
+    for kind in ("gS", "gD"):
+        for g, r in zip(got[kind], ref[kind]):
+            for b in range(r.shape[0]):
+                assert np.max(np.abs(g[b] - r[b])) <= GRAD_FRAC * np.max(np.abs(r[b]))
+
+
+def test_noalloc_matches_stage3_on_two_calls_in_a_row():
+    p = Params(weight=(1.0, 4.0))
+    first = S.make_inputs(3, [50_003, 701], "bf16", S.STAGE3, seed=(900,))
+    second = S.make_inputs(5, [20_011, 1_999], "bf16", S.STAGE3, seed=(901,))
+    for inp in (first, second):
+        _same(_run(inp, p, noalloc=True), _run(inp, p, noalloc=False), "bf16")
+
+
+def test_noalloc_rejects_a_batch_beyond_its_scratch():
+    inp = S.make_inputs(1, [64, 16], "bf16", S.STAGE3, seed=(902,))
+    big = 1
+    while t2va.workspace_bytes(big, 2) <= t2va.binding.NOALLOC_SCRATCH_BYTES:
+        big *= 2
+    z = [torch.zeros((big, 64), dtype=torch.bfloat16, device="cuda"),
+         torch.zeros((big, 16), dtype=torch.bfloat16, device="cuda")]
+    g = grads_like(z)
+    t = torch.full((big,), 0.5, device="cuda")
+    loss = torch.zeros(big, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(t2va.T2VAError) as e:
+        t2va.stage3_objective_noalloc(z, z, z, z, t, z, z, z, beta=1, gamma=0.9, eps_scm=1e-6,
+                                      eps_dmd=1e-6, weight=[1, 1], lambda_scm=1, lambda_dmd=0.25,
+                                      grad_x0_student=g, grad_zhat0=g, loss=loss, status=status)
+    assert e.value.code == 4
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    del inp
