@@ -16,6 +16,7 @@ namespace {
 struct DeviceInfo {
   int sm_count = 0;
   size_t smem_optin = 0;
+  size_t l2_bytes = 0;
   bool valid = false;
 };
 
@@ -32,14 +33,16 @@ bool current_device(DeviceInfo* out) {
   std::lock_guard<std::mutex> lock(g_devices_mu);
   DeviceInfo& d = g_devices[dev];
   if (!d.valid) {
-    int sms = 0, optin = 0;
+    int sms = 0, optin = 0, l2 = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) {
       cudaGetLastError();
       return false;
     }
     d.sm_count = sms;
     d.smem_optin = (size_t)optin;
+    d.l2_bytes = (size_t)l2;
     d.valid = sms > 0;
   }
   *out = d;
@@ -102,11 +105,19 @@ int run_objective(ObjectiveArgs& a, t2va_dtype dt, int mode, void* workspace, si
   if (workspace == nullptr || !aligned(workspace, 16) || ws_size < need) return T2VA_ERROR_WORKSPACE;
   unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
   a.hdr = reinterpret_cast<WsHeader*>(ws);
-  a.sync = reinterpret_cast<uint32_t*>(ws + kWsHeaderBytes);
-  a.partials = reinterpret_cast<float*>(ws + ws_partials_offset(a.B));
+  a.partials = reinterpret_cast<uint64_t*>(ws + kWsHeaderBytes);
   a.gmax = dev.sm_count;
+  for (int m = 0; m < a.M; ++m) {
+    const bool s_ok = a.grad_s[m] == nullptr || aligned(a.grad_s[m], 32);
+    const bool d_ok = a.grad_d[m] == nullptr || aligned(a.grad_d[m], 32);
+    // every full vector starts a multiple of 8 elements from the buffer's start (the
+    // unaligned head of a sample is done element by element), so 32-byte aligned
+    // buffers give 32-byte aligned 8-float gradient runs
+    if (s_ok && d_ok) a.wide_mask |= 1u << m;
+  }
   ObjectiveLaunch l;
-  if (!plan_objective(a, dt, mode, dev.sm_count, dev.smem_optin, &l)) return T2VA_ERROR_CUDA;
+  if (!plan_objective(a, dt, mode, dev.sm_count, dev.smem_optin, dev.l2_bytes, &l))
+    return T2VA_ERROR_CUDA;
   const cudaError_t e = launch_objective(a, dt, mode, l, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -2,6 +2,7 @@
 // joint video-audio distillation objective library (sm_103a).
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -15,33 +16,32 @@ constexpr uint32_t kWsMagic = 0x54325641u;  // "T2VA"
 
 // ---------------------------------------------------------------------------
 // Workspace layout (caller-owned device memory, prepared by t2va_workspace_init)
-//   [0, 256)                header
-//   [256, 256 + 64*B)       per-round arrival counters, one per 64 bytes (rounds <= B)
-//   then                    partial sums float[B][M][3][gmax]
+//   [0, 256)     header
+//   [256, ...)   partial sums, one 64-bit word per (sample, modality, quantity, CTA):
+//                low half the float32 bits of the CTA's sum, high half the epoch of
+//                the call that wrote it. A word is final for a call exactly when its
+//                epoch is that call's epoch, so the cross-CTA wait and the merge are
+//                one read of the words, and nothing has to be reset between calls.
 // ---------------------------------------------------------------------------
 struct WsHeader {
   uint32_t magic;
   uint32_t poisoned;     // set by a kernel that timed out; refused until re-initialised
   uint64_t timeout_ns;
-  uint32_t gmax;         // partial-sum slots per (sample, modality, quantity)
-  uint32_t exit_count;   // CTAs that finished the current call; the last one resets the counters
-  uint32_t pad[58];
+  uint32_t gmax;         // partial-sum words per (sample, modality, quantity)
+  uint32_t epoch;        // epoch of the next call (never 0); advanced by CTA 0 of every call
+  uint32_t withhold_cta; // test hook: this CTA publishes no sums, so every wait runs out
+                         // (0xFFFFFFFF, the value set by t2va_workspace_init, disables it)
+  uint32_t pad[57];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
+static_assert(offsetof(WsHeader, withhold_cta) == 24, "header layout");
 
 constexpr size_t kWsHeaderBytes = 256;
-constexpr size_t kWsSyncBytesPerSample = 64;
 constexpr int kQuantities = 3;  // sum g_sCM^2, sum |zhat0 - y_T|, sum g_DMD^2
 
 inline size_t ws_bytes(int B, int M, int gmax) {
-  size_t sync = (size_t)B * kWsSyncBytesPerSample;
-  size_t partial = (size_t)B * M * kQuantities * gmax * sizeof(float);
-  return kWsHeaderBytes + ((sync + 255) / 256) * 256 + ((partial + 255) / 256) * 256;
-}
-
-inline size_t ws_partials_offset(int B) {
-  size_t sync = (size_t)B * kWsSyncBytesPerSample;
-  return kWsHeaderBytes + ((sync + 255) / 256) * 256;
+  size_t partial = (size_t)B * M * kQuantities * gmax * sizeof(uint64_t);
+  return kWsHeaderBytes + ((partial + 255) / 256) * 256;
 }
 
 // Modes of the objective kernel.
@@ -62,25 +62,24 @@ struct ObjectiveArgs {
   float w[kMaxM];
   int accumulate;
   uint32_t alias_mask;         // bit m: grad_d[m] == grad_s[m], write the sum once
+  uint32_t wide_mask;          // bit m: the gradient buffers of m are 32-byte aligned
   float* loss;
   float* loss_s;
   float* loss_d;
   float* norm;
   float* cdmd;
   WsHeader* hdr;
-  uint32_t* sync;              // arrival counter of round r at sync[16 r]
-  float* partials;
+  uint64_t* partials;          // epoch-tagged words [B][M][3][gmax]
   int gmax;
   int* status;
   // launch plan (filled by plan_objective)
-  int groups;                  // 2: round r+1 is read while round r waits; 1: no overlap
+  int groups;                  // 2: round r+1 is read before round r's gradients are written
   int spr;                     // samples per round
   int rounds;
   int64_t chunk[kMaxM];        // vectors of one (sample, modality) owned by each CTA
-  int iters[kMaxM];            // ceil(chunk / threads)
-  int64_t cap[kMaxM];          // vectors per (sample, modality) kept in shared memory
-  int64_t choff[kMaxM];        // float4 offset of modality m inside one sample's region
-  int64_t sample_f4;           // float4 per sample region
+  int choff[kMaxM];            // first slot of modality m in a sample's slot range (multiple of 32)
+  int sample_f;                // slots per sample: sum over m of chunk[m] rounded up to 32
+  int keep_f;                  // slots per sample whose directions stay in shared memory
 };
 
 struct NoiseArgs {
@@ -105,10 +104,10 @@ struct ObjectiveLaunch {
   int threads;
   size_t smem;
 };
-// Chooses the grid and the round plan for `a` (fills the plan fields); returns
-// false if the device cannot run it.
+// Chooses the grid, the ring depth and the rounds for `a` (fills the plan fields);
+// returns false if the device cannot run it.
 bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int mode, int sm_count, size_t smem_optin,
-                    ObjectiveLaunch* out);
+                    size_t l2_bytes, ObjectiveLaunch* out);
 cudaError_t launch_objective(const ObjectiveArgs& a, t2va_dtype dt, int mode,
                              const ObjectiveLaunch& l, cudaStream_t st);
 cudaError_t launch_workspace_init(void* ws, size_t bytes, uint64_t timeout_ns, uint32_t gmax,

@@ -117,10 +117,18 @@ __global__ void __launch_bounds__(kNoiseThreads) k_noise(const __grid_constant__
 int noise_vectors_per_cta() { return kNoiseVecPerCta; }
 
 cudaError_t launch_noise(const NoiseArgs& a, t2va_dtype dt, int grid, cudaStream_t st) {
-  if (dt == T2VA_BFLOAT16)
+  // The kernel uses no shared memory; asking for the largest shared-memory carveout
+  // anyway lets the objective kernel that usually follows (which needs most of it)
+  // start without reconfiguring the SMs.
+  if (dt == T2VA_BFLOAT16) {
+    cudaFuncSetAttribute(k_noise<__nv_bfloat16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
     k_noise<__nv_bfloat16><<<grid, kNoiseThreads, 0, st>>>(a);
-  else
+  } else {
+    cudaFuncSetAttribute(k_noise<float>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
     k_noise<float><<<grid, kNoiseThreads, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -2,26 +2,32 @@
 // reading: section 3.1 joint sCM, section 四 joint DMD, section 4.1 stage-3 sum;
 // robotworld.top/en summary: Eq. 6 and Eq. 11-12).
 //
-// Design (one persistent launch, one CTA per SM, all CTAs co-resident):
+// Design (one persistent cooperative launch, one CTA of 512 threads per SM):
 //   Every (sample, modality) segment is cut into G equal chunks of 16-byte vectors,
-//   one per CTA, so every segment is spread over the whole GPU and the small audio
-//   segment never leaves SMs idle. Samples are processed in rounds of `spr`
-//   samples that share one cross-CTA barrier:
-//   Phase A(r): stream the round's inputs once (16-byte loads, the next item's
-//     loads in flight while the current one computes), compute the float32
-//     directions g_sCM and g_DMD, keep them in shared memory, and accumulate the
-//     per-(sample, modality) sums  sum g_sCM^2, sum |zhat0 - y_T|, sum g_DMD^2.
-//     Each CTA writes its sums to the workspace and adds 1 to the round's counter.
-//   Wait(r): a bounded poll until the counter reaches G; every CTA then merges the
-//     per-CTA sums itself in a fixed order (identical, run-to-run reproducible
-//     totals in every CTA) and derives the per-(sample, modality) gradient factor.
-//   Phase W(r): scale the kept directions and write the float32 gradients once.
-//   With two shared-memory groups the order is A0 A1 W0 A2 W1 ... so each round's
-//   barrier is hidden behind the next round's reads. Vectors that do not fit in
-//   shared memory are recomputed from the inputs in phase W. The last CTA to
-//   finish resets the counters for the next call.
-// HBM traffic is therefore the algorithmic minimum whenever one sample's
-// directions fit on chip: each input read once, each gradient written once.
+//   one per CTA, so each segment is spread over the whole GPU and the small audio
+//   segment never leaves SMs idle. Inside a CTA, the chunks of one sample are laid
+//   end to end in a "slot" range (each modality's chunk padded to a multiple of 32,
+//   so a warp's 32 consecutive slots always belong to one modality); thread t owns
+//   slots t, t + 512, ... of every sample. Samples are processed in rounds of `spr`:
+//   A(r): stream the round's inputs once with 16-byte loads, keeping the next slot's
+//     loads in flight while the current slot is computed (also across sample and
+//     round boundaries). Compute the float32 directions g_sCM and g_DMD, keep them in
+//     shared memory, and accumulate per-(sample, modality) sums of g_sCM^2,
+//     |zhat0 - y_T| and g_DMD^2 per warp. The CTA then publishes its sums as 64-bit
+//     words tagged with the call's epoch.
+//   Merge(r): every CTA reads all CTAs' words of the round in parallel, waiting (with
+//     a time limit) until every word carries this call's epoch, and adds them in a
+//     fixed order: every CTA gets bit-identical totals, run to run.
+//   W(r): scale the kept directions by the per-(sample, modality) factors and write
+//     the float32 gradients once.
+//   When all samples fit in shared memory there is one round (A, merge, W). Otherwise
+//   rounds alternate between two shared-memory groups in the order A0 A1 W0 A2 W1 ...
+//   so each merge is waited for behind the next round's reads. Slots that do not fit
+//   in shared memory (one sample larger than the GPU's shared memory) are recomputed
+//   from the inputs in W.
+// HBM traffic is the algorithmic minimum whenever one sample's directions fit on
+// chip: each input read once, each gradient written once. The epoch tags replace
+// arrival counters, so nothing needs resetting between calls.
 #include <algorithm>
 
 #include "t2va_internal.cuh"
@@ -31,7 +37,8 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxRound = 8;  // samples per round
+constexpr int kMaxRound = 8;          // samples per round
+constexpr uint32_t kNoWithhold = 0xFFFFFFFFu;
 
 struct RoundCoef {
   float kD, kz, kx, s;
@@ -39,15 +46,16 @@ struct RoundCoef {
 };
 
 struct SmemCtl {
-  float red[kWarps][kMaxRound][kMaxM][kQuantities];
-  float scal[kMaxRound][kMaxM][kQuantities];
-  float tot[2][kMaxRound][kMaxM][kQuantities];
+  float red[kWarps][kMaxRound][kMaxM][kQuantities];  // per-warp sums of the current round
+  float scal[kMaxRound][kMaxM][kQuantities];         // unaligned head/tail sums (CTA G-1)
+  float tot[2][kMaxRound][kMaxM][kQuantities];       // merged totals of a round
   float scaleS[2][kMaxRound][kMaxM];
   float scaleD[2][kMaxRound][kMaxM];
   RoundCoef coef[2][kMaxRound];
   uint64_t timeout_ns;
+  uint32_t epoch;
+  uint32_t withhold;
   int abort;
-  int checked;
 };
 constexpr size_t kCtlBytes = (sizeof(SmemCtl) + 15) / 16 * 16;
 
@@ -56,12 +64,36 @@ struct Traits {
   static constexpr int VE = Vec<T>::VE;
   static constexpr bool kScm = (MODE & kModeScm) != 0;
   static constexpr bool kDmd = (MODE & kModeDmd) != 0;
+  // float4 pieces of kept direction per vector
+  static constexpr int kPieces = ((kScm ? 1 : 0) + (kDmd ? 1 : 0)) * VE / 4;
 };
 
 template <typename T, int MODE>
 struct Loaded {
   uint4 r[kNumInputs];
 };
+
+// ---------------------------------------------------------------------------
+// epoch-tagged partial sums
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint64_t ld_word(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_word(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t pack_word(float v, uint32_t epoch) {
+  return ((uint64_t)epoch << 32) | (uint64_t)__float_as_uint(v);
+}
+
+// ---------------------------------------------------------------------------
+// per-vector arithmetic
+// ---------------------------------------------------------------------------
 
 template <typename T, int MODE>
 __device__ __forceinline__ void load_vec(Loaded<T, MODE>& L, const ObjectiveArgs& a, int m,
@@ -127,56 +159,62 @@ __device__ __forceinline__ float sum16(float v) {
   return v;
 }
 
-// One work item of a thread: vector k*threads + tid of this CTA's chunk of the
-// (sample b0 + bl, modality m) segment.
+// ---------------------------------------------------------------------------
+// slots
+// ---------------------------------------------------------------------------
+
+// One slot of a thread: sample bl of round r, slot index inside that sample.
 struct Item {
-  int bl, m, k;
+  int r, bl, slot;
 };
 
-struct ItemInfo {
-  int64_t e;    // first element of the vector
-  int64_t pos;  // position inside the CTA's chunk (shared-memory slot)
+__device__ __forceinline__ int round_size(const ObjectiveArgs& a, int r) {
+  return min(a.spr, a.B - r * a.spr);
+}
+
+// The thread's first slot of round r; false if it owns no slot at all (every
+// thread owns the same number of slots in every sample, which may be zero).
+__device__ __forceinline__ bool item_begin(Item& it, int r, const ObjectiveArgs& a) {
+  it.r = r;
+  it.bl = 0;
+  it.slot = threadIdx.x;
+  return r < a.rounds && (int)threadIdx.x < a.sample_f;
+}
+
+// The thread's next slot, in this sample, the next sample or the next round.
+__device__ __forceinline__ bool item_next(Item& it, const ObjectiveArgs& a) {
+  it.slot += kThreads;
+  if (it.slot < a.sample_f) return true;
+  it.slot = threadIdx.x;
+  if (++it.bl < round_size(a, it.r)) return true;
+  it.bl = 0;
+  return ++it.r < a.rounds;
+}
+
+struct Where {
+  int64_t e;  // first element of the vector
+  int m;
   bool valid;
 };
 
-// Advance to the next (bl, m, k) with k < iters[m]; false when the round is done.
-__device__ __forceinline__ bool next_item(Item& it, int nb, const ObjectiveArgs& a) {
-  if (++it.k < a.iters[it.m]) return true;
-  it.k = 0;
-  for (;;) {
-    if (++it.m == a.M) {
-      it.m = 0;
-      if (++it.bl == nb) return false;
-    }
-    if (a.iters[it.m] > 0) return true;
-  }
-}
-
-__device__ __forceinline__ bool first_item(Item& it, int nb, const ObjectiveArgs& a) {
-  it.bl = 0;
-  it.k = 0;
-  for (it.m = 0; it.m < a.M; ++it.m)
-    if (a.iters[it.m] > 0) return nb > 0;
-  return false;
-}
-
 template <int VE>
-__device__ __forceinline__ ItemInfo item_info(const Item& it, int b0, int cta, const ObjectiveArgs& a) {
-  const SegGeom g = seg_geom<VE>(a.n[it.m], a.stride[it.m], b0 + it.bl);
-  const int64_t chunk = a.chunk[it.m];
-  const int64_t lo = (int64_t)cta * chunk;
-  const int64_t pos = (int64_t)it.k * kThreads + threadIdx.x;
-  const int64_t v = lo + pos;
-  const int64_t vend = min(lo + chunk, g.nvec);
-  ItemInfo r;
-  r.valid = v < vend;
-  r.pos = pos;
-  r.e = g.e0 + g.head + v * VE;
-  return r;
+__device__ __forceinline__ Where locate(const Item& it, int cta, const ObjectiveArgs& a) {
+  int m = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxM; ++i)
+    if (i < a.M && it.slot >= a.choff[i]) m = i;
+  const int64_t pos = it.slot - a.choff[m];
+  const SegGeom g = seg_geom<VE>(a.n[m], a.stride[m], it.r * a.spr + it.bl);
+  const int64_t v = (int64_t)cta * a.chunk[m] + pos;
+  Where w;
+  w.m = m;
+  w.valid = pos < a.chunk[m] && v < g.nvec;
+  w.e = g.e0 + g.head + v * VE;
+  return w;
 }
 
 template <typename T, int MODE>
-__device__ __forceinline__ void keep(float4* region, int64_t cap, int64_t pos, const float* gs,
+__device__ __forceinline__ void keep(float4* region, int64_t stride, int64_t pos, const float* gs,
                                      const float* gd) {
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
@@ -184,17 +222,17 @@ __device__ __forceinline__ void keep(float4* region, int64_t cap, int64_t pos, c
   if constexpr (Tr::kScm) {
 #pragma unroll
     for (int i = 0; i < VE; i += 4, ++p)
-      region[p * cap + pos] = make_float4(gs[i], gs[i + 1], gs[i + 2], gs[i + 3]);
+      region[p * stride + pos] = make_float4(gs[i], gs[i + 1], gs[i + 2], gs[i + 3]);
   }
   if constexpr (Tr::kDmd) {
 #pragma unroll
     for (int i = 0; i < VE; i += 4, ++p)
-      region[p * cap + pos] = make_float4(gd[i], gd[i + 1], gd[i + 2], gd[i + 3]);
+      region[p * stride + pos] = make_float4(gd[i], gd[i + 1], gd[i + 2], gd[i + 3]);
   }
 }
 
 template <typename T, int MODE>
-__device__ __forceinline__ void fetch(const float4* region, int64_t cap, int64_t pos, float* gs,
+__device__ __forceinline__ void fetch(const float4* region, int64_t stride, int64_t pos, float* gs,
                                       float* gd) {
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
@@ -202,23 +240,28 @@ __device__ __forceinline__ void fetch(const float4* region, int64_t cap, int64_t
   if constexpr (Tr::kScm) {
 #pragma unroll
     for (int i = 0; i < VE; i += 4, ++p) {
-      const float4 f = region[p * cap + pos];
+      const float4 f = region[p * stride + pos];
       gs[i] = f.x; gs[i + 1] = f.y; gs[i + 2] = f.z; gs[i + 3] = f.w;
     }
   }
   if constexpr (Tr::kDmd) {
 #pragma unroll
     for (int i = 0; i < VE; i += 4, ++p) {
-      const float4 f = region[p * cap + pos];
+      const float4 f = region[p * stride + pos];
       gd[i] = f.x; gd[i + 1] = f.y; gd[i + 2] = f.z; gd[i + 3] = f.w;
     }
   }
 }
 
-// The unaligned head and tail elements of every (sample, modality) segment of the
-// round are handled by CTA G-1, one element per thread: 16 threads per segment
-// (at most 7 head + 7 tail elements), at most kMaxRound * kMaxM = 32 segments.
-// Returns the element index, or -1 if this thread has none; sets the slot (bl, m).
+// ---------------------------------------------------------------------------
+// unaligned head and tail elements
+// ---------------------------------------------------------------------------
+
+// The elements before the first 16-byte boundary and after the last full vector of
+// every (sample, modality) segment of the round are handled by CTA G-1, one element
+// per thread: 16 threads per segment (at most 7 head + 7 tail elements), at most
+// kMaxRound * kMaxM = 32 segments. Returns the element index, or -1 if this thread
+// has none; sets the segment (bl, m).
 template <int VE>
 __device__ __forceinline__ int64_t scalar_element(const ObjectiveArgs& a, int b0, int nb, int& bl,
                                                   int& m) {
@@ -253,32 +296,33 @@ __device__ __forceinline__ void scalar_direction(const ObjectiveArgs& a, int m, 
   }
 }
 
+// ---------------------------------------------------------------------------
+// round set-up, publication, merge
+// ---------------------------------------------------------------------------
+
+// Per-sample coefficients of round r and the head/tail sums (CTA G-1).
 template <typename T, int MODE>
-__device__ void phase_a(const ObjectiveArgs& a, SmemCtl& ctl, float4* group, int r, int cta, int G) {
+__device__ void round_setup(const ObjectiveArgs& a, SmemCtl& ctl, int r, int cta, int G) {
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int gi = r % a.groups;
+  const int tid = threadIdx.x;
+  const int ci = r & 1;
   const int b0 = r * a.spr;
-  const int nb = min(a.spr, a.B - b0);
-
-  if (r >= a.groups) __syncthreads();  // this group's buffers were last read in W(r - groups)
+  const int nb = round_size(a, r);
   if (tid < nb) {
     RoundCoef c{0.f, 0.f, 0.f, 1.f, 1};
     if constexpr (Tr::kScm) {
       const Coef k = sample_coef(__ldg(a.t + b0 + tid), a.beta, a.gamma);
       c = RoundCoef{k.kD, k.kz, k.kx, k.s, k.ok ? 1 : 0};
     }
-    ctl.coef[gi][tid] = c;
+    ctl.coef[ci][tid] = c;
   }
   __syncthreads();
-
-  // unaligned head/tail elements (CTA G-1 only; block-uniform branch)
-  if (cta == G - 1) {
+  if (cta == G - 1) {  // block-uniform
     int bl, m;
     const int64_t e = scalar_element<VE>(a, b0, nb, bl, m);
     float gs = 0.f, gd = 0.f, sabs = 0.f;
-    if (e >= 0) scalar_direction<T, MODE>(a, m, e, ctl.coef[gi][bl], gs, gd, sabs);
+    if (e >= 0) scalar_direction<T, MODE>(a, m, e, ctl.coef[ci][bl], gs, gd, sabs);
     const float sg = sum16(gs * gs), sa = sum16(sabs), sd = sum16(gd * gd);
     if ((tid & 15) == 0 && bl < nb) {
       ctl.scal[bl][m][0] = sg;
@@ -286,137 +330,128 @@ __device__ void phase_a(const ObjectiveArgs& a, SmemCtl& ctl, float4* group, int
       ctl.scal[bl][m][2] = sd;
     }
   }
+}
 
-  // this CTA's vectors of every segment of the round; the next item's loads are in
-  // flight while the current item is computed
-  Item it;
-  bool more = first_item(it, nb, a);
-  Loaded<T, MODE> Lc;
-  ItemInfo ic{0, 0, false};
-  if (more) {
-    ic = item_info<VE>(it, b0, cta, a);
-    if (ic.valid) load_vec<T, MODE>(Lc, a, it.m, ic.e);
-  }
-  float sg = 0.f, sa = 0.f, sd = 0.f;
-  while (more) {
-    Item nx = it;
-    const bool more_n = next_item(nx, nb, a);
-    Loaded<T, MODE> Ln;
-    ItemInfo in{0, 0, false};
-    if (more_n) {
-      in = item_info<VE>(nx, b0, cta, a);
-      if (in.valid) load_vec<T, MODE>(Ln, a, nx.m, in.e);
-    }
-    if (ic.valid) {
-      float gs[VE], gd[VE];
-      directions<T, MODE>(Lc, ctl.coef[gi][it.bl], gs, gd, sg, sa, sd);
-      if (ic.pos < a.cap[it.m])
-        keep<T, MODE>(group + it.bl * a.sample_f4 + a.choff[it.m], a.cap[it.m], ic.pos, gs, gd);
-    }
-    if (!more_n || nx.bl != it.bl || nx.m != it.m) {  // end of a segment (warp-uniform)
-      sg = warp_sum(sg);
-      sa = warp_sum(sa);
-      sd = warp_sum(sd);
-      if (lane == 0) {
-        ctl.red[warp][it.bl][it.m][0] = sg;
-        ctl.red[warp][it.bl][it.m][1] = sa;
-        ctl.red[warp][it.bl][it.m][2] = sd;
-      }
-      sg = sa = sd = 0.f;
-    }
-    it = nx;
-    ic = in;
-    Lc = Ln;
-    more = more_n;
-  }
-  __syncthreads();
-
-  // CTA sums -> workspace, then one arrival on the round's counter (no wait here)
-  if (warp == 0) {
-    if (tid == 0 && !ctl.checked) {
-      const uint32_t magic = ld_relaxed_gpu(&a.hdr->magic);
-      const uint32_t poisoned = ld_relaxed_gpu(&a.hdr->poisoned);
-      ctl.timeout_ns = *reinterpret_cast<volatile uint64_t*>(&a.hdr->timeout_ns);
-      ctl.checked = 1;
-      if (magic != kWsMagic || poisoned != 0) {
-        ctl.abort = 1;
-        atomicOr(a.status, T2VA_STATUS_BAD_WORKSPACE);
-      }
-    }
-    __syncwarp();
-    if (!ctl.abort) {
-      const int per_bl = a.M * kQuantities;
-      for (int u = lane; u < nb * per_bl; u += 32) {
-        const int bl = u / per_bl;
-        const int m = (u - bl * per_bl) / kQuantities;
-        const int q = u - bl * per_bl - m * kQuantities;
-        float s = 0.f;
-        if (a.iters[m] > 0) {
-#pragma unroll
-          for (int w = 0; w < kWarps; ++w) s += ctl.red[w][bl][m][q];
-        }
-        if (cta == G - 1) s += ctl.scal[bl][m][q];
-        a.partials[(((int64_t)(b0 + bl) * a.M + m) * kQuantities + q) * a.gmax + cta] = s;
-      }
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence();
-        atomicAdd(a.sync + (int64_t)r * 16, 1u);
-      }
+// After A(r): the CTA's sums of every (sample, modality, quantity) of the round, as
+// epoch-tagged words. The per-warp partials are added in a fixed order.
+__device__ void publish(const ObjectiveArgs& a, SmemCtl& ctl, int r, int cta, int G) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b0 = r * a.spr;
+  const int nb = round_size(a, r);
+  const int rows = nb * a.M * kQuantities;
+  for (int u = warp; u < rows; u += kWarps) {
+    const int bl = u / (a.M * kQuantities);
+    const int m = (u / kQuantities) % a.M;
+    const int q = u % kQuantities;
+    float s = lane < kWarps ? ctl.red[lane][bl][m][q] : 0.f;
+    s = warp_sum(s);
+    if (lane == 0) {
+      if (cta == G - 1) s += ctl.scal[bl][m][q];
+      if ((uint32_t)cta != ctl.withhold)
+        st_word(a.partials + (((int64_t)(b0 + bl) * a.M + m) * kQuantities + q) * a.gmax + cta,
+                pack_word(s, ctl.epoch));
     }
   }
 }
 
-// Bounded wait for every CTA's sums of round r, then the fixed-order merge and the
-// per-(sample, modality) gradient factors.
+// Merge(r): wait (bounded) until every CTA's words of round r carry this call's epoch,
+// add them in CTA order, and derive the per-(sample, modality) gradient factors. A
+// warp reads the words of up to kRowsPerPass rows at once, so one round trip to L2
+// serves all of them.
+constexpr int kRowsPerPass = 3;
+constexpr int kWordsPerLane = 5;   // CTAs 32 j + lane, j < 5: 160 CTAs per pass
+
 template <typename T, int MODE>
-__device__ bool wait_and_merge(const ObjectiveArgs& a, SmemCtl& ctl, int r, int G) {
+__device__ bool merge(const ObjectiveArgs& a, SmemCtl& ctl, int r, int G) {
   using Tr = Traits<T, MODE>;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int gi = r % a.groups;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ci = r & 1;
   const int b0 = r * a.spr;
-  const int nb = min(a.spr, a.B - b0);
-  if (tid == 0 && !ctl.abort) {
-    const uint32_t* cnt = a.sync + (int64_t)r * 16;
-    const uint64_t start = global_timer_ns();
-    // signed: a counter that holds a negative value never reaches G (the timeout test's planted state)
-    while ((int32_t)ld_acquire_gpu(cnt) < G) {
-      if (global_timer_ns() - start > ctl.timeout_ns) {
-        ctl.abort = 1;
-        atomicOr(a.status, T2VA_STATUS_TIMEOUT);
-        atomicExch(&a.hdr->poisoned, 1u);
-        break;
-      }
-    }
-    __threadfence();
-  }
-  __syncthreads();
-  if (ctl.abort) return false;
-  const int per_bl = a.M * kQuantities;
+  const int nb = round_size(a, r);
+  const int rows = nb * a.M * kQuantities;
+  const uint32_t E = ctl.epoch;
   const float qnan = __int_as_float(0x7fc00000);
-  for (int u = warp; u < nb * per_bl; u += kWarps) {
-    const int bl = u / per_bl;
-    const int m = (u - bl * per_bl) / kQuantities;
-    const int q = u - bl * per_bl - m * kQuantities;
-    const float* src = a.partials + (((int64_t)(b0 + bl) * a.M + m) * kQuantities + q) * a.gmax;
-    float s = 0.f;
-    for (int i = lane; i < G; i += 32) s += __ldcg(src + i);
-    s = warp_sum(s);
-    if (lane == 0) {
-      ctl.tot[gi][bl][m][q] = s;
-      const RoundCoef& k = ctl.coef[gi][bl];
-      if (Tr::kScm && q == 0) {
-        const float n = sqrtf(s);
-        ctl.scaleS[gi][bl][m] = 2.f * a.lam_s * a.w[m] / (k.s * (n + a.eps_s));
+  for (int u0 = warp; u0 < rows; u0 += kWarps * kRowsPerPass) {
+    float s[kRowsPerPass];
+#pragma unroll
+    for (int i = 0; i < kRowsPerPass; ++i) s[i] = 0.f;
+    for (int base = 0; base < G; base += 32 * kWordsPerLane) {
+      uint64_t w[kRowsPerPass][kWordsPerLane];
+      uint64_t start = 0;
+      for (;;) {
+        bool ready = true;
+#pragma unroll
+        for (int i = 0; i < kRowsPerPass; ++i) {
+          const int u = u0 + i * kWarps;
+          const uint64_t* src = a.partials + ((int64_t)b0 * a.M * kQuantities + u) * a.gmax;
+#pragma unroll
+          for (int j = 0; j < kWordsPerLane; ++j) {
+            const int c = base + lane + 32 * j;
+            w[i][j] = (u < rows && c < G) ? ld_word(src + c) : pack_word(0.f, E);
+            ready &= (uint32_t)(w[i][j] >> 32) == E;
+          }
+        }
+        if (__all_sync(0xffffffffu, ready)) break;
+        const uint64_t now = global_timer_ns();
+        if (start == 0) start = now;
+        if (now - start > ctl.timeout_ns || *reinterpret_cast<volatile int*>(&ctl.abort)) {
+          if (lane == 0 && !*reinterpret_cast<volatile int*>(&ctl.abort)) {
+            ctl.abort = 1;
+            atomicOr(a.status, T2VA_STATUS_TIMEOUT);
+            atomicExch(&a.hdr->poisoned, 1u);
+          }
+          break;
+        }
       }
-      if (Tr::kDmd && q == 1) {
-        const float c = a.n[m] > 0 ? s / (float)a.n[m] : 0.f;
-        ctl.scaleD[gi][bl][m] = k.ok ? 2.f * a.lam_d * a.w[m] / (c + a.eps_d) : qnan;
+#pragma unroll
+      for (int i = 0; i < kRowsPerPass; ++i)
+#pragma unroll
+        for (int j = 0; j < kWordsPerLane; ++j) s[i] += __uint_as_float((uint32_t)w[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < kRowsPerPass; ++i) {
+      const int u = u0 + i * kWarps;
+      const float tot = warp_sum(s[i]);
+      if (lane == 0 && u < rows) {
+        const int bl = u / (a.M * kQuantities);
+        const int m = (u / kQuantities) % a.M;
+        const int q = u % kQuantities;
+        ctl.tot[ci][bl][m][q] = tot;
+        const RoundCoef& k = ctl.coef[ci][bl];
+        if (Tr::kScm && q == 0) {
+          const float n = sqrtf(tot);
+          ctl.scaleS[ci][bl][m] = 2.f * a.lam_s * a.w[m] / (k.s * (n + a.eps_s));
+        }
+        if (Tr::kDmd && q == 1) {
+          const float c = a.n[m] > 0 ? tot / (float)a.n[m] : 0.f;
+          ctl.scaleD[ci][bl][m] = k.ok ? 2.f * a.lam_d * a.w[m] / (c + a.eps_d) : qnan;
+        }
       }
     }
   }
   __syncthreads();
-  return true;
+  return !ctl.abort;
+}
+
+// ---------------------------------------------------------------------------
+// gradients
+// ---------------------------------------------------------------------------
+
+// Eight consecutive gradients (32 bytes, 32-byte aligned) in one store, so every
+// store instruction of a warp writes whole 32-byte sectors.
+__device__ __forceinline__ void write8(float* dst, const float* v, int accumulate) {
+  float o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i] = v[i];
+  if (accumulate) {
+    const float4* d = reinterpret_cast<const float4*>(dst);
+    const float4 a0 = d[0], a1 = d[1];
+    o[0] += a0.x; o[1] += a0.y; o[2] += a0.z; o[3] += a0.w;
+    o[4] += a1.x; o[5] += a1.y; o[6] += a1.z; o[7] += a1.w;
+  }
+  asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "f"(o[0]),
+               "f"(o[1]), "f"(o[2]), "f"(o[3]), "f"(o[4]), "f"(o[5]), "f"(o[6]), "f"(o[7])
+               : "memory");
 }
 
 __device__ __forceinline__ void write4(float* dst, float4 o, int accumulate) {
@@ -434,6 +469,28 @@ __device__ __forceinline__ void write_vec(const ObjectiveArgs& a, int m, int64_t
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
   const bool alias = Tr::kScm && Tr::kDmd && ((a.alias_mask >> m) & 1u);
+  if constexpr (VE == 8) {
+    if ((a.wide_mask >> m) & 1u) {  // both gradient buffers of m are 32-byte aligned
+      float o[8];
+      if (alias) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = scS * gs[i] + scD * gd[i];
+        write8(a.grad_s[m] + e, o, a.accumulate);
+        return;
+      }
+      if constexpr (Tr::kScm) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = scS * gs[i];
+        write8(a.grad_s[m] + e, o, a.accumulate);
+      }
+      if constexpr (Tr::kDmd) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = scD * gd[i];
+        write8(a.grad_d[m] + e, o, a.accumulate);
+      }
+      return;
+    }
+  }
 #pragma unroll
   for (int i = 0; i < VE; i += 4) {
     if (alias) {
@@ -459,36 +516,39 @@ __device__ __forceinline__ void write1(float* dst, float v, int accumulate) {
   *dst = v;
 }
 
+// W(r): the gradients of round r and its per-sample outputs.
 template <typename T, int MODE>
-__device__ void phase_w(const ObjectiveArgs& a, SmemCtl& ctl, const float4* group, int r, int cta,
-                        int G) {
+__device__ void write_round(const ObjectiveArgs& a, SmemCtl& ctl, const float4* group, int r,
+                            int cta, int G) {
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
   const int tid = threadIdx.x;
-  const int gi = r % a.groups;
+  const int ci = r & 1;
   const int b0 = r * a.spr;
-  const int nb = min(a.spr, a.B - b0);
+  const int nb = round_size(a, r);
+  const int64_t kstride = (int64_t)a.spr * a.keep_f;
   const float qnan = __int_as_float(0x7fc00000);
 
-  Item it;
-  bool more = first_item(it, nb, a);
-  while (more) {
-    const ItemInfo ic = item_info<VE>(it, b0, cta, a);
-    if (ic.valid) {
-      float gs[VE], gd[VE];
-      if (ic.pos < a.cap[it.m]) {
-        fetch<T, MODE>(group + it.bl * a.sample_f4 + a.choff[it.m], a.cap[it.m], ic.pos, gs, gd);
-      } else {  // not kept on chip: recompute from the inputs
-        Loaded<T, MODE> L;
-        load_vec<T, MODE>(L, a, it.m, ic.e);
-        float d0 = 0.f, d1 = 0.f, d2 = 0.f;
-        directions<T, MODE>(L, ctl.coef[gi][it.bl], gs, gd, d0, d1, d2);
+  if (tid < a.sample_f) {
+    for (int bl = 0; bl < nb; ++bl) {
+      for (int slot = tid; slot < a.sample_f; slot += kThreads) {
+        const Item it{r, bl, slot};
+        const Where w = locate<VE>(it, cta, a);
+        if (!w.valid) continue;
+        float gs[VE], gd[VE];
+        if (slot < a.keep_f) {
+          fetch<T, MODE>(group, kstride, (int64_t)bl * a.keep_f + slot, gs, gd);
+        } else {  // not kept on chip: recompute from the inputs
+          Loaded<T, MODE> L;
+          load_vec<T, MODE>(L, a, w.m, w.e);
+          float d0 = 0.f, d1 = 0.f, d2 = 0.f;
+          directions<T, MODE>(L, ctl.coef[ci][bl], gs, gd, d0, d1, d2);
+        }
+        const float scS = Tr::kScm ? ctl.scaleS[ci][bl][w.m] : 0.f;
+        const float scD = Tr::kDmd ? ctl.scaleD[ci][bl][w.m] : 0.f;
+        write_vec<T, MODE>(a, w.m, w.e, scS, scD, gs, gd);
       }
-      const float scS = Tr::kScm ? ctl.scaleS[gi][it.bl][it.m] : 0.f;
-      const float scD = Tr::kDmd ? ctl.scaleD[gi][it.bl][it.m] : 0.f;
-      write_vec<T, MODE>(a, it.m, ic.e, scS, scD, gs, gd);
     }
-    more = next_item(it, nb, a);
   }
 
   // unaligned head/tail elements (CTA G-1)
@@ -497,9 +557,9 @@ __device__ void phase_w(const ObjectiveArgs& a, SmemCtl& ctl, const float4* grou
     const int64_t e = scalar_element<VE>(a, b0, nb, bl, m);
     if (e >= 0) {
       float gs = 0.f, gd = 0.f, sabs = 0.f;
-      scalar_direction<T, MODE>(a, m, e, ctl.coef[gi][bl], gs, gd, sabs);
-      const float scS = Tr::kScm ? ctl.scaleS[gi][bl][m] : 0.f;
-      const float scD = Tr::kDmd ? ctl.scaleD[gi][bl][m] : 0.f;
+      scalar_direction<T, MODE>(a, m, e, ctl.coef[ci][bl], gs, gd, sabs);
+      const float scS = Tr::kScm ? ctl.scaleS[ci][bl][m] : 0.f;
+      const float scD = Tr::kDmd ? ctl.scaleD[ci][bl][m] : 0.f;
       if (Tr::kScm && Tr::kDmd && ((a.alias_mask >> m) & 1u)) {
         write1(a.grad_s[m] + e, scS * gs + scD * gd, a.accumulate);
       } else {
@@ -513,20 +573,20 @@ __device__ void phase_w(const ObjectiveArgs& a, SmemCtl& ctl, const float4* grou
   for (int bl = tid; bl < nb; bl += kThreads) {
     const int b = b0 + bl;
     if (b % G != cta) continue;
-    const RoundCoef& k = ctl.coef[gi][bl];
+    const RoundCoef& k = ctl.coef[ci][bl];
     float Ls = 0.f, Ld = 0.f;
     for (int m = 0; m < a.M; ++m) {
       if constexpr (Tr::kScm) {
-        const float Sg = ctl.tot[gi][bl][m][0];
+        const float Sg = ctl.tot[ci][bl][m][0];
         const float n = sqrtf(Sg);
         const float d = n + a.eps_s;
         Ls += a.w[m] * (Sg / (d * d));
         if (a.norm) a.norm[(int64_t)b * a.M + m] = k.ok ? n : qnan;
       }
       if constexpr (Tr::kDmd) {
-        const float c = a.n[m] > 0 ? ctl.tot[gi][bl][m][1] / (float)a.n[m] : 0.f;
+        const float c = a.n[m] > 0 ? ctl.tot[ci][bl][m][1] / (float)a.n[m] : 0.f;
         const float d = c + a.eps_d;
-        Ld += a.w[m] * (ctl.tot[gi][bl][m][2] / (d * d));
+        Ld += a.w[m] * (ctl.tot[ci][bl][m][2] / (d * d));
         if (a.cdmd) a.cdmd[(int64_t)b * a.M + m] = k.ok ? c : qnan;
       }
     }
@@ -543,41 +603,117 @@ __device__ void phase_w(const ObjectiveArgs& a, SmemCtl& ctl, const float4* grou
   }
 }
 
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) k_objective(const __grid_constant__ ObjectiveArgs a) {
+  using Tr = Traits<T, MODE>;
+  constexpr int VE = Tr::VE;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(smem_raw);
-  float4* groups = reinterpret_cast<float4*>(smem_raw + kCtlBytes);
-  const int64_t group_f4 = (int64_t)a.spr * a.sample_f4;
+  float4* kept = reinterpret_cast<float4*>(smem_raw + kCtlBytes);
+  const int64_t kstride = (int64_t)a.spr * a.keep_f;  // float4 per piece of one group
+  const int64_t group_f4 = (int64_t)Tr::kPieces * kstride;
   const int G = gridDim.x, cta = blockIdx.x;
-  if (threadIdx.x == 0) {
-    ctl.abort = 0;
-    ctl.checked = 0;
-  }
-  __syncthreads();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  const int K = a.groups;
+  if (tid == 0) {
+    const uint32_t magic = ld_relaxed_gpu(&a.hdr->magic);
+    const uint32_t poisoned = ld_relaxed_gpu(&a.hdr->poisoned);
+    ctl.timeout_ns = *reinterpret_cast<volatile uint64_t*>(&a.hdr->timeout_ns);
+    ctl.epoch = ld_relaxed_gpu(&a.hdr->epoch);
+    ctl.withhold = ld_relaxed_gpu(&a.hdr->withhold_cta);
+    ctl.abort = 0;
+    if (magic != kWsMagic || poisoned != 0 || ctl.epoch == 0) {
+      ctl.abort = 1;
+      atomicOr(a.status, T2VA_STATUS_BAD_WORKSPACE);
+    }
+  }
+  for (int u = lane; u < kMaxRound * kMaxM * kQuantities; u += 32)
+    (&ctl.red[warp][0][0][0])[u] = 0.f;
+  __syncthreads();
+  if (ctl.abort) return;
+
+  // the first slot's loads
+  Item it;
+  bool have = item_begin(it, 0, a);
+  Loaded<T, MODE> Lc;
+  Where wc{0, 0, false};
+  if (have) {
+    wc = locate<VE>(it, cta, a);
+    if (wc.valid) load_vec<T, MODE>(Lc, a, wc.m, wc.e);
+  }
+
   for (int r = 0; r < a.rounds; ++r) {
-    phase_a<T, MODE>(a, ctl, groups + (r % K) * group_f4, r, cta, G);
-    const int wr = (K == 1) ? r : r - 1;
-    if (wr >= 0) {
-      if (!wait_and_merge<T, MODE>(a, ctl, wr, G)) return;
-      phase_w<T, MODE>(a, ctl, groups + (wr % K) * group_f4, wr, cta, G);
+    const int ci = r & 1;
+    __syncthreads();  // the previous round's W (and reads of its group) are done
+    round_setup<T, MODE>(a, ctl, r, cta, G);
+    __syncthreads();
+    float4* group = kept + (r % a.groups) * group_f4;
+
+    // A(r): the next slot's loads are in flight while this one is computed
+    float sg = 0.f, sa = 0.f, sd = 0.f;
+    while (have && it.r == r) {
+      Item nx = it;
+      const bool have_n = item_next(nx, a);
+      Loaded<T, MODE> Ln;
+      Where wn{0, 0, false};
+      if (have_n) {
+        wn = locate<VE>(nx, cta, a);
+        if (wn.valid) load_vec<T, MODE>(Ln, a, wn.m, wn.e);
+      }
+      if (wc.valid) {
+        float gs[VE], gd[VE];
+        directions<T, MODE>(Lc, ctl.coef[ci][it.bl], gs, gd, sg, sa, sd);
+        if (it.slot < a.keep_f)
+          keep<T, MODE>(group, kstride, (int64_t)it.bl * a.keep_f + it.slot, gs, gd);
+      }
+      // a warp's slots change (sample, modality) together: flush its sums then
+      if (!have_n || nx.r != r || nx.bl != it.bl || wn.m != wc.m) {
+        sg = warp_sum(sg);
+        sa = warp_sum(sa);
+        sd = warp_sum(sd);
+        if (lane == 0) {
+          ctl.red[warp][it.bl][wc.m][0] += sg;
+          ctl.red[warp][it.bl][wc.m][1] += sa;
+          ctl.red[warp][it.bl][wc.m][2] += sd;
+        }
+        sg = sa = sd = 0.f;
+      }
+      it = nx;
+      Lc = Ln;
+      wc = wn;
+      have = have_n;
+    }
+    __syncthreads();  // per-warp sums and head/tail sums complete
+    publish(a, ctl, r, cta, G);
+    __syncthreads();  // sums read: clear this warp's rows for the next round
+    for (int u = lane; u < kMaxRound * kMaxM * kQuantities; u += 32)
+      (&ctl.red[warp][0][0][0])[u] = 0.f;
+
+    if (a.groups == 1) {
+      if (!merge<T, MODE>(a, ctl, r, G)) return;
+      write_round<T, MODE>(a, ctl, group, r, cta, G);
+    } else if (r >= 1) {
+      if (!merge<T, MODE>(a, ctl, r - 1, G)) return;
+      write_round<T, MODE>(a, ctl, kept + ((r - 1) % a.groups) * group_f4, r - 1, cta, G);
     }
   }
-  if (K > 1 && a.rounds > 0) {
-    const int wr = a.rounds - 1;
-    if (!wait_and_merge<T, MODE>(a, ctl, wr, G)) return;
-    phase_w<T, MODE>(a, ctl, groups + (wr % K) * group_f4, wr, cta, G);
+  if (a.groups > 1 && a.rounds > 0) {
+    const int r = a.rounds - 1;
+    if (!merge<T, MODE>(a, ctl, r, G)) return;
+    write_round<T, MODE>(a, ctl, kept + (r % a.groups) * group_f4, r, cta, G);
   }
-  // The last CTA to get here resets the round counters for the next call: every
-  // other CTA finished all of its waits before counting itself out.
-  if (threadIdx.x == 0) {
-    const uint32_t old = atomicAdd(&a.hdr->exit_count, 1u);
-    if (old == (uint32_t)(G - 1)) {
-      for (int r = 0; r < a.rounds; ++r) a.sync[(int64_t)r * 16] = 0u;
-      a.hdr->exit_count = 0u;
-    }
+  // Every CTA has published its last round's words, tagged with this epoch, before
+  // CTA 0's last merge could finish: all of them have read the epoch, so it can move
+  // on for the next call.
+  if (cta == 0 && tid == 0) {
+    const uint32_t next = ctl.epoch + 1u;
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(&a.hdr->epoch),
+                 "r"(next == 0u ? 1u : next)
+                 : "memory");
   }
 }
 
@@ -610,7 +746,8 @@ __global__ void k_ws_init(uint4* ws, size_t n16, uint64_t timeout_ns, uint32_t g
     h->timeout_ns = timeout_ns;
     h->gmax = gmax;
     h->poisoned = 0;
-    h->exit_count = 0;
+    h->epoch = 1;  // zeroed words carry epoch 0, so no word of a fresh workspace is final
+    h->withhold_cta = kNoWithhold;
     __threadfence();
     h->magic = kWsMagic;
   }
@@ -619,10 +756,10 @@ __global__ void k_ws_init(uint4* ws, size_t n16, uint64_t timeout_ns, uint32_t g
 }  // namespace
 
 bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int mode, int sm_count, size_t smem_optin,
-                    ObjectiveLaunch* out) {
+                    size_t /*l2_bytes*/, ObjectiveLaunch* out) {
   const int VE = dt == T2VA_BFLOAT16 ? 8 : 4;
   const int Q = ((mode & kModeScm) ? 1 : 0) + ((mode & kModeDmd) ? 1 : 0);
-  const int64_t P = (int64_t)Q * VE / 4;  // float4 pieces kept per vector
+  const int64_t slot_bytes = (int64_t)Q * VE / 4 * 16;  // kept direction bytes per slot
   int64_t vtot = 0, nvec_ub[kMaxM];
   for (int m = 0; m < a.M; ++m) {
     nvec_ub[m] = (a.n[m] + VE - 1) / VE;
@@ -630,42 +767,41 @@ bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int mode, int sm_count, siz
   }
   int64_t G = (vtot + kThreads - 1) / kThreads;  // small problems use fewer CTAs
   G = std::max<int64_t>(1, std::min<int64_t>({G, (int64_t)sm_count, (int64_t)a.gmax}));
-  int64_t per_sample_f4 = 0;
+  int64_t acc = 0;
   for (int m = 0; m < a.M; ++m) {
     a.chunk[m] = (nvec_ub[m] + G - 1) / G;
-    const int64_t it = (a.chunk[m] + kThreads - 1) / kThreads;
-    if (it > INT32_MAX) return false;
-    a.iters[m] = (int)it;
-    per_sample_f4 += P * a.chunk[m];
+    a.choff[m] = (int)std::min<int64_t>(acc, INT32_MAX);
+    acc += (a.chunk[m] + 31) / 32 * 32;
+    if (acc > (int64_t)1 << 30) return false;
   }
-  if (smem_optin <= kCtlBytes + 16 * (size_t)P) return false;
-  const int64_t budget_f4 = (int64_t)((smem_optin - kCtlBytes) / 16);
-  int64_t keep_num = 1, keep_den = 1;  // fraction of each chunk kept on chip
-  if (a.B >= 2 && 2 * per_sample_f4 <= budget_f4) {
-    a.groups = 2;
-    const int64_t spr = std::min<int64_t>(budget_f4 / (2 * per_sample_f4), (a.B + 1) / 2);
-    a.spr = (int)std::max<int64_t>(1, std::min<int64_t>(spr, kMaxRound));
-  } else if (per_sample_f4 <= budget_f4) {
-    a.groups = 1;
-    const int64_t spr = per_sample_f4 > 0 ? std::min<int64_t>(budget_f4 / per_sample_f4, a.B) : a.B;
-    a.spr = (int)std::max<int64_t>(1, std::min<int64_t>(spr, kMaxRound));
-  } else {
+  for (int m = a.M; m < kMaxM; ++m) {
+    a.chunk[m] = 0;
+    a.choff[m] = (int)acc;
+  }
+  a.sample_f = (int)acc;
+  if (smem_optin <= kCtlBytes + (size_t)32 * slot_bytes) return false;
+  const int64_t budget = (int64_t)(smem_optin - kCtlBytes);
+  const int64_t per_sample = a.sample_f * slot_bytes;
+  a.keep_f = a.sample_f;
+  if (per_sample == 0 || (a.B <= kMaxRound && a.B * per_sample <= budget)) {
+    a.groups = 1;  // one round: A, merge, W
+    a.spr = std::max(1, std::min(a.B, kMaxRound));
+  } else if (a.B >= 2 && 2 * per_sample <= budget) {
+    a.groups = 2;  // A0 A1 W0 A2 W1 ...
+    const int64_t spr = std::min<int64_t>({budget / (2 * per_sample), (a.B + 1) / 2, kMaxRound});
+    a.spr = (int)std::max<int64_t>(1, spr);
+  } else if (per_sample <= budget) {
     a.groups = 1;
     a.spr = 1;
-    keep_num = budget_f4;
-    keep_den = per_sample_f4;
+  } else {  // one sample's directions exceed shared memory: keep a prefix of its slots
+    a.groups = 1;
+    a.spr = 1;
+    a.keep_f = (int)(budget / slot_bytes / 32 * 32);
   }
-  int64_t off = 0;
-  for (int m = 0; m < a.M; ++m) {
-    a.cap[m] = a.chunk[m] * keep_num / keep_den;
-    a.choff[m] = off;
-    off += P * a.cap[m];
-  }
-  a.sample_f4 = off;
   a.rounds = (a.B + a.spr - 1) / a.spr;
   out->grid = (int)G;
   out->threads = kThreads;
-  out->smem = kCtlBytes + (size_t)a.groups * a.spr * a.sample_f4 * 16;
+  out->smem = kCtlBytes + (size_t)a.groups * a.spr * a.keep_f * slot_bytes;
   return true;
 }
 

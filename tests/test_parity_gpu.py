@@ -293,14 +293,16 @@ def test_cuda_graph_capture_matches_eager():
 # --------------------------------------------------------------------------
 
 def test_timeout_sets_status_and_poisons_workspace():
-    """A corrupted arrival counter means no CTA ever sees the last arrival; every wait
-    gives up after the workspace's limit (200 ms here), sets TIMEOUT and returns. The
-    workspace then refuses work until it is initialised again."""
+    """The workspace header's withhold field (32-bit word 6 of the header) names a CTA
+    that publishes no partial sums, so no CTA ever sees all of them: every wait gives
+    up after the workspace's limit (200 ms here), sets TIMEOUT and returns. The
+    workspace then refuses work until it is initialised again (which also clears the
+    field)."""
     inp = S.make_inputs(2, [50000, 500], "bf16", S.STAGE3, seed=(400,))
     p = Params()
     ws = t2va.new_workspace(2, 2, timeout_ms=200)
     torch.cuda.synchronize()
-    ws.view(torch.int32)[64] = -(1 << 30)   # round 0's arrival counter: G arrivals never reach G
+    ws.view(torch.int32)[6] = 0   # CTA 0 withholds its sums
     bad = gpu_run(inp, p, S.STAGE3, workspace=ws)
     assert bad["status"] & t2va.STATUS_TIMEOUT
     again = gpu_run(inp, p, S.STAGE3, workspace=ws)
