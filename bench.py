@@ -319,7 +319,7 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
         else:
             t2va.noise(d["z0"], d["eps"], d["zt"], d["t"], status=status, stream=stream)
 
-    launches_per_step = 2
+    launches_per_step = 3   # t2va_noise + the objective's two kernels
 
     # CUDA graphs of whole steps, with no event nodes inside: an event node between two
     # kernels of a graph costs about 3 us of its own, which would be charged to the step
@@ -433,7 +433,8 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
                    "clock_ramp_s": args.clock_ramp_seconds},
         "elements_per_s": nb["elements"] * world * K / (elapsed_ms * 1e-3),
         "hbm_fraction_of_step": round(value / world / peak, 4),
-        "roofline": {"kernel": "t2va stage-3 objective" if wl.mode == S.STAGE3 else "t2va sCM objective",
+        "roofline": {"kernel": ("t2va stage-3 objective" if wl.mode == S.STAGE3 else "t2va sCM objective")
+                               + " call (k_sums + k_grads)",
                      "bound": "hbm", "achieved": round(obj_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(obj_gbs / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6400 GB/s",

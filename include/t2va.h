@@ -34,9 +34,8 @@
  * - Inputs are float32 or bfloat16 (`dtype`); arithmetic is float32 with
  *   float32 accumulation; gradients are written in float32.
  * - The caller owns every buffer and the stream. The library allocates no
- *   device memory, keeps no state across calls except inside the caller's
- *   workspace, and never synchronises the host: calls are asynchronous on
- *   `stream`. Outputs must not overlap inputs.
+ *   device memory, keeps no state across calls, and never synchronises the
+ *   host: calls are asynchronous on `stream`. Outputs must not overlap inputs.
  * - Return value: T2VA_SUCCESS or a synchronous error code (argument checks,
  *   launch failure); nothing is enqueued when an error is returned. Problems
  *   found on the device set bits in the caller's device int `*status`
@@ -82,10 +81,10 @@ enum {
 
 /* Device status bits, OR-ed into *status by the kernels. */
 #define T2VA_STATUS_BAD_TIMESTEP 0x1  /* a sample's t is outside (0, pi/2): its outputs are NaN    */
-#define T2VA_STATUS_TIMEOUT 0x2       /* a cross-CTA wait ran out; outputs of the call are invalid
-                                         and the workspace must be re-initialised                 */
-#define T2VA_STATUS_BAD_WORKSPACE 0x4 /* the workspace was not initialised (or is poisoned by a
-                                         timeout); nothing was computed                          */
+/* Reserved (ABI version 1 kept them; no kernel of this library waits on another CTA or
+ * checks the workspace, so neither is ever set). */
+#define T2VA_STATUS_TIMEOUT 0x2
+#define T2VA_STATUS_BAD_WORKSPACE 0x4
 
 /* Static description of a return code (never NULL). */
 const char* t2va_error_string(int code);
@@ -94,17 +93,18 @@ const char* t2va_error_string(int code);
 int t2va_abi_version(void);
 
 /* Bytes of workspace needed by the objective entry points for up to `batch`
- * samples of `num_modalities` modalities on the CURRENT device (the size
- * depends on its SM count). Returns 0 on invalid arguments or if no device
- * can be queried. */
+ * samples of `num_modalities` modalities: 256 bytes plus 16 KiB per (sample,
+ * modality). An objective call is two kernels on `stream`; the first writes
+ * per-chunk partial sums into the workspace and the second reads them, so the
+ * workspace needs no initialisation and keeps nothing between calls. Calls that
+ * may run concurrently need distinct workspaces. Returns 0 on invalid arguments
+ * or if no device can be queried. */
 size_t t2va_workspace_bytes(int batch, int num_modalities);
 
-/* Prepare a workspace (16-byte aligned device memory of `workspace_bytes`)
- * for use on `stream`: clears the cross-CTA counters and records the wait
- * limit `timeout_ms` (0 selects 1000 ms) after which a kernel gives up and
- * sets T2VA_STATUS_TIMEOUT instead of waiting on. Must be called once before
- * the first objective call that uses this workspace, and again after a
- * TIMEOUT. Calls that may run concurrently need distinct workspaces. */
+/* Zero a workspace (16-byte aligned device memory of `workspace_bytes`) on
+ * `stream` and write its header. Optional: the objective entry points do not
+ * depend on the workspace's contents. `timeout_ms` is recorded in the header
+ * for compatibility and not used. */
 int t2va_workspace_init(void* workspace, size_t workspace_bytes, uint32_t timeout_ms,
                         cudaStream_t stream);
 
@@ -137,8 +137,9 @@ int t2va_noise(int batch, int num_modalities, const t2va_segment* seg, t2va_dtyp
  * The whole g_bar is a stop-gradient target. Requires beta finite,
  * 0 <= gamma <= 1, eps_scm > 0, weight[m] >= 0. A sample with t outside
  * (0, pi/2) gets NaN outputs and sets T2VA_STATUS_BAD_TIMESTEP. `workspace`
- * must be initialised by t2va_workspace_init and hold
- * t2va_workspace_bytes(batch, M) bytes. `status` is required. */
+ * must hold t2va_workspace_bytes(batch, M) bytes (16-byte aligned). `status`
+ * is required. Runs as two kernels on `stream` (sums, then gradients); each
+ * input is read from HBM once when the call's inputs fit in L2, else twice. */
 int t2va_scm_objective(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
                        const void* const* z_t, const void* const* x0_teacher,
                        const void* const* x0_student, const void* const* x0_student_tangent,
@@ -170,8 +171,9 @@ int t2va_dmd_objective(int batch, int num_modalities, const t2va_segment* seg, t
 /* Stage-3 objective  ([zh] 4.1; [en] section 3):
  *   loss[b] = lambda_scm L_sCM,b + lambda_dmd L_DMD,b
  * over the same batch and the same per-sample t, with both terms as defined
- * above and one set of weights w_m. Reads the seven inputs once and writes both
- * gradients once, in one launch. `loss_scm` and `loss_dmd` (device float
+ * above and one set of weights w_m. Two kernels on `stream`: the first reads the
+ * seven inputs for the sums, the second reads them again (from L2 when they fit
+ * there) and writes both gradients once. `loss_scm` and `loss_dmd` (device float
  * [batch], each already multiplied by its lambda) may be NULL, as may `norm`
  * and `cdmd`. If grad_zhat0[m] == grad_x0_student[m] (the caller's on-policy
  * sample is the student output itself), the two gradients are summed into
@@ -209,20 +211,18 @@ int t2va_stage3_objective(int batch, int num_modalities, const t2va_segment* seg
  * device memory per GPU. The call allocates nothing: no cudaMalloc, no cudaFree
  * and no allocating library routine.
  *
- * - Limit: the workspace that `batch` and `num_modalities` need on the current
- *   device (t2va_workspace_bytes) must fit in the scratch. About 290 samples of
- *   2 modalities fit on a 148-SM GPU. A larger batch returns
- *   T2VA_ERROR_WORKSPACE, and nothing is enqueued.
+ * - Limit: the workspace that `batch` and `num_modalities` need
+ *   (t2va_workspace_bytes: 16 KiB per sample and modality) must fit in the
+ *   scratch, so at most 31 samples of 2 modalities per call. A larger batch
+ *   returns T2VA_ERROR_WORKSPACE, and nothing is enqueued.
  * - First call: the first call on each device, with that device current, looks
  *   up the scratch's device address (cudaGetSymbolAddress) and keeps it. Make
  *   that first call before any stream capture on that device.
- * - Sharing: every call on a device shares the one scratch array, which keeps
- *   what the last call left there. Each call first re-initialises the array's
- *   header and arrival counters with one small kernel on `stream`, then
- *   launches the objective. Calls that overlap on the GPU (on different streams
- *   or from different host threads) race on the array and give wrong results.
- *   Order them on one stream, or use t2va_stage3_objective with one workspace
- *   per concurrent call.
+ * - Sharing: every call on a device shares the one scratch array. A call's first
+ *   kernel writes the partial sums its second kernel reads, so the array needs no
+ *   clearing, but calls that overlap on the GPU (on different streams or from
+ *   different host threads) race on it and give wrong results. Order them on one
+ *   stream, or use t2va_stage3_objective with one workspace per concurrent call.
  * - Errors: argument errors are those of t2va_stage3_objective, returned before
  *   anything is enqueued. T2VA_ERROR_CUDA means the scratch's address could not
  *   be obtained. */

@@ -104,8 +104,7 @@ int run_objective(ObjectiveArgs& a, t2va_dtype dt, int mode, void* workspace, si
   const size_t need = ws_bytes(a.B, a.M, dev.sm_count);
   if (workspace == nullptr || !aligned(workspace, 16) || ws_size < need) return T2VA_ERROR_WORKSPACE;
   unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
-  a.hdr = reinterpret_cast<WsHeader*>(ws);
-  a.partials = reinterpret_cast<uint64_t*>(ws + kWsHeaderBytes);
+  a.partials = reinterpret_cast<float*>(ws + kWsHeaderBytes);
   a.gmax = dev.sm_count;
   for (int m = 0; m < a.M; ++m) {
     const bool s_ok = a.grad_s[m] == nullptr || aligned(a.grad_s[m], 32);

@@ -15,33 +15,27 @@ constexpr int kMaxM = T2VA_MAX_MODALITIES;
 constexpr uint32_t kWsMagic = 0x54325641u;  // "T2VA"
 
 // ---------------------------------------------------------------------------
-// Workspace layout (caller-owned device memory, prepared by t2va_workspace_init)
-//   [0, 256)     header
-//   [256, ...)   partial sums, one 64-bit word per (sample, modality, quantity, CTA):
-//                low half the float32 bits of the CTA's sum, high half the epoch of
-//                the call that wrote it. A word is final for a call exactly when its
-//                epoch is that call's epoch, so the cross-CTA wait and the merge are
-//                one read of the words, and nothing has to be reset between calls.
+// Workspace layout (caller-owned device memory)
+//   [0, 256)     header (written by t2va_workspace_init; the kernels do not need it)
+//   [256, ...)   partial sums: float4 {sum g_sCM^2, sum |zhat0 - y_T|, sum g_DMD^2, 0}
+//                per (sample, modality, chunk), kMaxChunks chunks per (sample, modality),
+//                written by the first kernel of a call and read by the second
 // ---------------------------------------------------------------------------
 struct WsHeader {
   uint32_t magic;
-  uint32_t poisoned;     // set by a kernel that timed out; refused until re-initialised
-  uint64_t timeout_ns;
-  uint32_t gmax;         // partial-sum words per (sample, modality, quantity)
-  uint32_t epoch;        // epoch of the next call (never 0); advanced by CTA 0 of every call
-  uint32_t withhold_cta; // test hook: this CTA publishes no sums, so every wait runs out
-                         // (0xFFFFFFFF, the value set by t2va_workspace_init, disables it)
-  uint32_t pad[57];
+  uint32_t reserved0;
+  uint64_t timeout_ns;   // recorded by t2va_workspace_init (no wait in the kernels uses it)
+  uint32_t gmax;
+  uint32_t pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
-static_assert(offsetof(WsHeader, withhold_cta) == 24, "header layout");
 
 constexpr size_t kWsHeaderBytes = 256;
 constexpr int kQuantities = 3;  // sum g_sCM^2, sum |zhat0 - y_T|, sum g_DMD^2
+constexpr int kMaxChunks = 1024;  // chunks per (sample, modality) row
 
-inline size_t ws_bytes(int B, int M, int gmax) {
-  size_t partial = (size_t)B * M * kQuantities * gmax * sizeof(uint64_t);
-  return kWsHeaderBytes + ((partial + 255) / 256) * 256;
+inline size_t ws_bytes(int B, int M, int /*sm_count*/) {
+  return kWsHeaderBytes + (size_t)B * M * kMaxChunks * 16;
 }
 
 // Modes of the objective kernel.
@@ -68,18 +62,13 @@ struct ObjectiveArgs {
   float* loss_d;
   float* norm;
   float* cdmd;
-  WsHeader* hdr;
-  uint64_t* partials;          // epoch-tagged words [B][M][3][gmax]
+  float* partials;             // float4 [B][M][kMaxChunks]
   int gmax;
   int* status;
   // launch plan (filled by plan_objective)
-  int groups;                  // 2: round r+1 is read before round r's gradients are written
-  int spr;                     // samples per round
-  int rounds;
-  int64_t chunk[kMaxM];        // vectors of one (sample, modality) owned by each CTA
-  int choff[kMaxM];            // first slot of modality m in a sample's slot range (multiple of 32)
-  int sample_f;                // slots per sample: sum over m of chunk[m] rounded up to 32
-  int keep_f;                  // slots per sample whose directions stay in shared memory
+  int vpc;                     // 16-byte vectors per chunk (a multiple of one CTA's batch)
+  int nchunk[kMaxM];           // chunks per (sample, modality m) row
+  int choff[kMaxM + 1];        // first chunk of modality m inside a sample; choff[M] = per sample
 };
 
 struct NoiseArgs {
@@ -104,8 +93,8 @@ struct ObjectiveLaunch {
   int threads;
   size_t smem;
 };
-// Chooses the grid, the ring depth and the rounds for `a` (fills the plan fields);
-// returns false if the device cannot run it.
+// Chooses the chunks and the grid for `a` (fills the plan fields); returns false if
+// the problem is too large for the workspace layout.
 bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int mode, int sm_count, size_t smem_optin,
                     size_t l2_bytes, ObjectiveLaunch* out);
 cudaError_t launch_objective(const ObjectiveArgs& a, t2va_dtype dt, int mode,

@@ -78,11 +78,8 @@ extern "C" int t2va_stage3_objective_noalloc(
   void* ws = nullptr;
   const int rc = scratch_address(&ws);
   if (rc != T2VA_SUCCESS) return rc;
-  // The array keeps whatever the last call left there, which may be a call with a
-  // different batch or a call that timed out. Clear the part this call uses and
-  // write a fresh header: one small kernel on `stream`.
-  const int init = t2va_workspace_init(ws, need, 0, stream);
-  if (init != T2VA_SUCCESS) return init;
+  // The array keeps whatever the last call left there; that is harmless, because the
+  // call's first kernel writes every partial sum its second kernel reads.
   return t2va_stage3_objective(batch, num_modalities, seg, dtype, z_t, x0_teacher, x0_student,
                                x0_student_tangent, t, zhat0, x0_teacher_hat, x0_fake, beta, gamma,
                                eps_scm, eps_dmd, weight, lambda_scm, lambda_dmd, grad_x0_student,

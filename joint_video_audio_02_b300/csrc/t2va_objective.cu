@@ -1,33 +1,28 @@
-// Fused joint sCM / DMD / stage-3 objective kernel (TurboT2VA, robotworld.top/zh
-// reading: section 3.1 joint sCM, section 四 joint DMD, section 4.1 stage-3 sum;
+// Joint sCM / DMD / stage-3 objective kernels (TurboT2VA, robotworld.top/zh reading:
+// section 3.1 joint sCM, section 四 joint DMD, section 4.1 stage-3 sum;
 // robotworld.top/en summary: Eq. 6 and Eq. 11-12).
 //
-// Design (one persistent cooperative launch, one CTA of 512 threads per SM):
-//   Every (sample, modality) segment is cut into G equal chunks of 16-byte vectors,
-//   one per CTA, so each segment is spread over the whole GPU and the small audio
-//   segment never leaves SMs idle. Inside a CTA, the chunks of one sample are laid
-//   end to end in a "slot" range (each modality's chunk padded to a multiple of 32,
-//   so a warp's 32 consecutive slots always belong to one modality); thread t owns
-//   slots t, t + 512, ... of every sample. Samples are processed in rounds of `spr`:
-//   A(r): stream the round's inputs once with 16-byte loads, keeping the next slot's
-//     loads in flight while the current slot is computed (also across sample and
-//     round boundaries). Compute the float32 directions g_sCM and g_DMD, keep them in
-//     shared memory, and accumulate per-(sample, modality) sums of g_sCM^2,
-//     |zhat0 - y_T| and g_DMD^2 per warp. The CTA then publishes its sums as 64-bit
-//     words tagged with the call's epoch.
-//   Merge(r): every CTA reads all CTAs' words of the round in parallel, waiting (with
-//     a time limit) until every word carries this call's epoch, and adds them in a
-//     fixed order: every CTA gets bit-identical totals, run to run.
-//   W(r): scale the kept directions by the per-(sample, modality) factors and write
-//     the float32 gradients once.
-//   When all samples fit in shared memory there is one round (A, merge, W). Otherwise
-//   rounds alternate between two shared-memory groups in the order A0 A1 W0 A2 W1 ...
-//   so each merge is waited for behind the next round's reads. Slots that do not fit
-//   in shared memory (one sample larger than the GPU's shared memory) are recomputed
-//   from the inputs in W.
-// HBM traffic is the algorithmic minimum whenever one sample's directions fit on
-// chip: each input read once, each gradient written once. The epoch tags replace
-// arrival counters, so nothing needs resetting between calls.
+// The gradient of every (sample, modality) needs that row's norms, which need all of
+// the row's elements, so the objective is two passes over the inputs, as two kernels
+// on the caller's stream; the kernel boundary is the only grid-wide barrier:
+//
+//   k_sums  : every (sample, modality) row is cut into chunks of `vpc` 16-byte
+//             vectors, one CTA per chunk (rows of every sample and modality in one
+//             grid, so the small audio rows share the GPU with the video rows). Each
+//             thread issues all the loads of its vectors at once, computes the float32
+//             directions g_sCM and g_DMD and accumulates sum g_sCM^2, sum |zhat0 - y_T|
+//             and sum g_DMD^2; the CTA adds them in a fixed order and writes the
+//             chunk's three partial sums to the workspace. The loads ask L2 to keep
+//             the inputs.
+//   k_grads : the same chunks. Each CTA starts the loads of its vectors again (L2
+//             hits; L2 may drop them now), adds the row's partial sums in chunk order
+//             (every CTA of a row gets bit-identical totals), derives the gradient
+//             factors, recomputes the directions and writes the float32 gradients
+//             once. The first chunk of each sample also writes the per-sample outputs.
+//
+// HBM sees each input read once and each gradient written once when a call's inputs
+// fit in L2 (126 MB on B300; the stage-3 512x768 batch of 4 reads 45 MB); larger
+// calls read the inputs twice. There is no cross-CTA wait, so nothing can hang.
 #include <algorithm>
 
 #include "t2va_internal.cuh"
@@ -35,96 +30,159 @@
 namespace t2va {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxRound = 8;          // samples per round
-constexpr uint32_t kNoWithhold = 0xFFFFFFFFu;
-
-struct RoundCoef {
-  float kD, kz, kx, s;
-  int ok;
-};
-
-struct SmemCtl {
-  float red[kWarps][kMaxRound][kMaxM][kQuantities];  // per-warp sums of the current round
-  float scal[kMaxRound][kMaxM][kQuantities];         // unaligned head/tail sums (CTA G-1)
-  float tot[2][kMaxRound][kMaxM][kQuantities];       // merged totals of a round
-  float scaleS[2][kMaxRound][kMaxM];
-  float scaleD[2][kMaxRound][kMaxM];
-  RoundCoef coef[2][kMaxRound];
-  uint64_t timeout_ns;
-  uint32_t epoch;
-  uint32_t withhold;
-  int abort;
-};
-constexpr size_t kCtlBytes = (sizeof(SmemCtl) + 15) / 16 * 16;
+constexpr int kPerThread = 2;                    // vectors per thread per batch
+constexpr int kBatchVec = kThreads * kPerThread;  // vectors per CTA per batch
 
 template <typename T, int MODE>
 struct Traits {
   static constexpr int VE = Vec<T>::VE;
   static constexpr bool kScm = (MODE & kModeScm) != 0;
   static constexpr bool kDmd = (MODE & kModeDmd) != 0;
-  // float4 pieces of kept direction per vector
-  static constexpr int kPieces = ((kScm ? 1 : 0) + (kDmd ? 1 : 0)) * VE / 4;
-};
-
-template <typename T, int MODE>
-struct Loaded {
-  uint4 r[kNumInputs];
+  static constexpr int k0 = kScm ? kZt : kZh;  // first input slot of the mode
+  static constexpr int NIN = (kScm ? 4 : 0) + (kDmd ? 3 : 0);
 };
 
 // ---------------------------------------------------------------------------
-// epoch-tagged partial sums
+// loads, cache policies, reductions
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ uint64_t ld_word(const uint64_t* p) {
-  uint64_t v;
-  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 16-byte streaming load through the read-only path, not kept in L1, with an L2
+// eviction policy.
+__device__ __forceinline__ uint4 ld16(const void* p, uint64_t policy) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(policy));
+  return r;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
   return v;
 }
 
-__device__ __forceinline__ void st_word(uint64_t* p, uint64_t v) {
-  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+// Sum of the CTA's three values in a fixed order: lanes, then warps. Every thread
+// gets the result.
+__device__ __forceinline__ float3 block_sum3(float a, float b, float c, float3 (&scratch)[kWarps]) {
+  a = warp_sum(a);
+  b = warp_sum(b);
+  c = warp_sum(c);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) scratch[warp] = make_float3(a, b, c);
+  __syncthreads();
+  float3 t = make_float3(0.f, 0.f, 0.f);
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    t.x += scratch[w].x;
+    t.y += scratch[w].y;
+    t.z += scratch[w].z;
+  }
+  __syncthreads();  // scratch may be reused
+  return t;
 }
 
-__device__ __forceinline__ uint64_t pack_word(float v, uint32_t epoch) {
-  return ((uint64_t)epoch << 32) | (uint64_t)__float_as_uint(v);
+// ---------------------------------------------------------------------------
+// chunks
+// ---------------------------------------------------------------------------
+
+// Chunk `blk`: sample b, modality m, chunk c of row (b, m), and the row's vectors
+// [v_lo, v_hi) that it owns (aligned vectors of the segment; element 0 of vector 0
+// is e_vec0).
+struct Chunk {
+  int b, m, c;
+  int64_t e_vec0, v_lo, v_hi;
+  SegGeom g;
+};
+
+template <int VE>
+__device__ __forceinline__ Chunk chunk_of(const ObjectiveArgs& a, int blk) {
+  Chunk k;
+  const int cps = a.choff[a.M];  // chunks per sample
+  k.b = blk / cps;
+  const int local = blk - k.b * cps;
+  k.m = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxM; ++i)
+    if (i < a.M && local >= a.choff[i]) k.m = i;
+  k.c = local - a.choff[k.m];
+  k.g = seg_geom<VE>(a.n[k.m], a.stride[k.m], k.b);
+  k.e_vec0 = k.g.e0 + k.g.head;
+  k.v_lo = (int64_t)k.c * a.vpc;
+  k.v_hi = min(k.v_lo + (int64_t)a.vpc, k.g.nvec);
+  return k;
+}
+
+__device__ __forceinline__ float4* row_partials(const ObjectiveArgs& a, int b, int m) {
+  return reinterpret_cast<float4*>(a.partials) + ((int64_t)b * a.M + m) * kMaxChunks;
+}
+
+// The unaligned head (chunk 0) and tail (last chunk) elements of a row: at most 7 of
+// each, one per thread: threads 0-6 take the head, threads 32-38 the tail.
+template <int VE>
+__device__ __forceinline__ int64_t edge_element(const ObjectiveArgs& a, const Chunk& k) {
+  const int t = threadIdx.x;
+  if (k.c == 0 && t < k.g.head) return k.g.e0 + t;
+  if (k.c == a.nchunk[k.m] - 1 && t >= 32 && t - 32 < k.g.tail)
+    return k.g.e0 + k.g.head + k.g.nvec * VE + (t - 32);
+  return -1;
 }
 
 // ---------------------------------------------------------------------------
 // per-vector arithmetic
 // ---------------------------------------------------------------------------
 
+struct Coefs {
+  float kD, kz, kx, s;
+  bool ok;
+};
+
 template <typename T, int MODE>
-__device__ __forceinline__ void load_vec(Loaded<T, MODE>& L, const ObjectiveArgs& a, int m,
-                                         int64_t e) {
-  using Tr = Traits<T, MODE>;
-  if constexpr (Tr::kScm) {
-    L.r[kZt] = ld_stream16(reinterpret_cast<const T*>(a.in[kZt][m]) + e);
-    L.r[kXT] = ld_stream16(reinterpret_cast<const T*>(a.in[kXT][m]) + e);
-    L.r[kXS] = ld_stream16(reinterpret_cast<const T*>(a.in[kXS][m]) + e);
-    L.r[kXdot] = ld_stream16(reinterpret_cast<const T*>(a.in[kXdot][m]) + e);
+__device__ __forceinline__ Coefs coefs_of(const ObjectiveArgs& a, int b) {
+  Coefs c{0.f, 0.f, 0.f, 1.f, true};
+  if constexpr (Traits<T, MODE>::kScm) {
+    const Coef k = sample_coef(__ldg(a.t + b), a.beta, a.gamma);
+    c = Coefs{k.kD, k.kz, k.kx, k.s, k.ok};
   }
-  if constexpr (Tr::kDmd) {
-    L.r[kZh] = ld_stream16(reinterpret_cast<const T*>(a.in[kZh][m]) + e);
-    L.r[kYT] = ld_stream16(reinterpret_cast<const T*>(a.in[kYT][m]) + e);
-    L.r[kYF] = ld_stream16(reinterpret_cast<const T*>(a.in[kYF][m]) + e);
-  }
+  return c;
 }
 
-// Directions of one vector: gs (sCM) and gd (DMD), and the three sums.
 template <typename T, int MODE>
-__device__ __forceinline__ void directions(const Loaded<T, MODE>& L, const RoundCoef& k,
-                                           float* gs, float* gd, float& sg, float& sa,
-                                           float& sd) {
+__device__ __forceinline__ void load_vec(uint4 (&in)[Traits<T, MODE>::NIN], const ObjectiveArgs& a,
+                                         int m, int64_t e, uint64_t policy) {
+  using Tr = Traits<T, MODE>;
+#pragma unroll
+  for (int q = 0; q < Tr::NIN; ++q)
+    in[q] = ld16(reinterpret_cast<const T*>(a.in[Tr::k0 + q][m]) + e, policy);
+}
+
+// The directions of one vector from its inputs (raw 16-byte chunks, in input order
+// starting at Traits::k0), and its three sums.
+template <typename T, int MODE>
+__device__ __forceinline__ void directions(const uint4 (&in)[Traits<T, MODE>::NIN], const Coefs& k,
+                                           float* gs, float* gd, float& sg, float& sa, float& sd) {
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
   if constexpr (Tr::kScm) {
     Vec<T> z, xt, xs, xd;
-    z.from(L.r[kZt]);
-    xt.from(L.r[kXT]);
-    xs.from(L.r[kXS]);
-    xd.from(L.r[kXdot]);
+    z.from(in[kZt - Tr::k0]);
+    xt.from(in[kXT - Tr::k0]);
+    xs.from(in[kXS - Tr::k0]);
+    xd.from(in[kXdot - Tr::k0]);
 #pragma unroll
     for (int i = 0; i < VE; ++i) {
       const float g = fmaf(k.kD, xt.v[i] - xs.v[i], fmaf(k.kz, z.v[i], k.kx * xd.v[i]));
@@ -134,9 +192,9 @@ __device__ __forceinline__ void directions(const Loaded<T, MODE>& L, const Round
   }
   if constexpr (Tr::kDmd) {
     Vec<T> zh, yt, yf;
-    zh.from(L.r[kZh]);
-    yt.from(L.r[kYT]);
-    yf.from(L.r[kYF]);
+    zh.from(in[kZh - Tr::k0]);
+    yt.from(in[kYT - Tr::k0]);
+    yf.from(in[kYF - Tr::k0]);
 #pragma unroll
     for (int i = 0; i < VE; ++i) {
       const float g = yf.v[i] - yt.v[i];
@@ -147,137 +205,9 @@ __device__ __forceinline__ void directions(const Loaded<T, MODE>& L, const Round
   }
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
-  return v;
-}
-
-__device__ __forceinline__ float sum16(float v) {
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// ---------------------------------------------------------------------------
-// slots
-// ---------------------------------------------------------------------------
-
-// One slot of a thread: sample bl of round r, slot index inside that sample.
-struct Item {
-  int r, bl, slot;
-};
-
-__device__ __forceinline__ int round_size(const ObjectiveArgs& a, int r) {
-  return min(a.spr, a.B - r * a.spr);
-}
-
-// The thread's first slot of round r; false if it owns no slot at all (every
-// thread owns the same number of slots in every sample, which may be zero).
-__device__ __forceinline__ bool item_begin(Item& it, int r, const ObjectiveArgs& a) {
-  it.r = r;
-  it.bl = 0;
-  it.slot = threadIdx.x;
-  return r < a.rounds && (int)threadIdx.x < a.sample_f;
-}
-
-// The thread's next slot, in this sample, the next sample or the next round.
-__device__ __forceinline__ bool item_next(Item& it, const ObjectiveArgs& a) {
-  it.slot += kThreads;
-  if (it.slot < a.sample_f) return true;
-  it.slot = threadIdx.x;
-  if (++it.bl < round_size(a, it.r)) return true;
-  it.bl = 0;
-  return ++it.r < a.rounds;
-}
-
-struct Where {
-  int64_t e;  // first element of the vector
-  int m;
-  bool valid;
-};
-
-template <int VE>
-__device__ __forceinline__ Where locate(const Item& it, int cta, const ObjectiveArgs& a) {
-  int m = 0;
-#pragma unroll
-  for (int i = 1; i < kMaxM; ++i)
-    if (i < a.M && it.slot >= a.choff[i]) m = i;
-  const int64_t pos = it.slot - a.choff[m];
-  const SegGeom g = seg_geom<VE>(a.n[m], a.stride[m], it.r * a.spr + it.bl);
-  const int64_t v = (int64_t)cta * a.chunk[m] + pos;
-  Where w;
-  w.m = m;
-  w.valid = pos < a.chunk[m] && v < g.nvec;
-  w.e = g.e0 + g.head + v * VE;
-  return w;
-}
-
-template <typename T, int MODE>
-__device__ __forceinline__ void keep(float4* region, int64_t stride, int64_t pos, const float* gs,
-                                     const float* gd) {
-  using Tr = Traits<T, MODE>;
-  constexpr int VE = Tr::VE;
-  int p = 0;
-  if constexpr (Tr::kScm) {
-#pragma unroll
-    for (int i = 0; i < VE; i += 4, ++p)
-      region[p * stride + pos] = make_float4(gs[i], gs[i + 1], gs[i + 2], gs[i + 3]);
-  }
-  if constexpr (Tr::kDmd) {
-#pragma unroll
-    for (int i = 0; i < VE; i += 4, ++p)
-      region[p * stride + pos] = make_float4(gd[i], gd[i + 1], gd[i + 2], gd[i + 3]);
-  }
-}
-
-template <typename T, int MODE>
-__device__ __forceinline__ void fetch(const float4* region, int64_t stride, int64_t pos, float* gs,
-                                      float* gd) {
-  using Tr = Traits<T, MODE>;
-  constexpr int VE = Tr::VE;
-  int p = 0;
-  if constexpr (Tr::kScm) {
-#pragma unroll
-    for (int i = 0; i < VE; i += 4, ++p) {
-      const float4 f = region[p * stride + pos];
-      gs[i] = f.x; gs[i + 1] = f.y; gs[i + 2] = f.z; gs[i + 3] = f.w;
-    }
-  }
-  if constexpr (Tr::kDmd) {
-#pragma unroll
-    for (int i = 0; i < VE; i += 4, ++p) {
-      const float4 f = region[p * stride + pos];
-      gd[i] = f.x; gd[i + 1] = f.y; gd[i + 2] = f.z; gd[i + 3] = f.w;
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// unaligned head and tail elements
-// ---------------------------------------------------------------------------
-
-// The elements before the first 16-byte boundary and after the last full vector of
-// every (sample, modality) segment of the round are handled by CTA G-1, one element
-// per thread: 16 threads per segment (at most 7 head + 7 tail elements), at most
-// kMaxRound * kMaxM = 32 segments. Returns the element index, or -1 if this thread
-// has none; sets the segment (bl, m).
-template <int VE>
-__device__ __forceinline__ int64_t scalar_element(const ObjectiveArgs& a, int b0, int nb, int& bl,
-                                                  int& m) {
-  const int pair = threadIdx.x >> 4, lane16 = threadIdx.x & 15;
-  bl = pair / a.M;
-  m = pair - bl * a.M;
-  if (bl >= nb) return -1;
-  const SegGeom g = seg_geom<VE>(a.n[m], a.stride[m], b0 + bl);
-  if (lane16 < g.head) return g.e0 + lane16;
-  if (lane16 >= 8 && lane16 - 8 < g.tail) return g.e0 + g.head + g.nvec * VE + (lane16 - 8);
-  return -1;
-}
-
 template <typename T, int MODE>
 __device__ __forceinline__ void scalar_direction(const ObjectiveArgs& a, int m, int64_t e,
-                                                 const RoundCoef& k, float& gs, float& gd,
+                                                 const Coefs& k, float& gs, float& gd,
                                                  float& sabs) {
   using Tr = Traits<T, MODE>;
   if constexpr (Tr::kScm) {
@@ -296,147 +226,6 @@ __device__ __forceinline__ void scalar_direction(const ObjectiveArgs& a, int m, 
   }
 }
 
-// ---------------------------------------------------------------------------
-// round set-up, publication, merge
-// ---------------------------------------------------------------------------
-
-// Per-sample coefficients of round r and the head/tail sums (CTA G-1).
-template <typename T, int MODE>
-__device__ void round_setup(const ObjectiveArgs& a, SmemCtl& ctl, int r, int cta, int G) {
-  using Tr = Traits<T, MODE>;
-  constexpr int VE = Tr::VE;
-  const int tid = threadIdx.x;
-  const int ci = r & 1;
-  const int b0 = r * a.spr;
-  const int nb = round_size(a, r);
-  if (tid < nb) {
-    RoundCoef c{0.f, 0.f, 0.f, 1.f, 1};
-    if constexpr (Tr::kScm) {
-      const Coef k = sample_coef(__ldg(a.t + b0 + tid), a.beta, a.gamma);
-      c = RoundCoef{k.kD, k.kz, k.kx, k.s, k.ok ? 1 : 0};
-    }
-    ctl.coef[ci][tid] = c;
-  }
-  __syncthreads();
-  if (cta == G - 1) {  // block-uniform
-    int bl, m;
-    const int64_t e = scalar_element<VE>(a, b0, nb, bl, m);
-    float gs = 0.f, gd = 0.f, sabs = 0.f;
-    if (e >= 0) scalar_direction<T, MODE>(a, m, e, ctl.coef[ci][bl], gs, gd, sabs);
-    const float sg = sum16(gs * gs), sa = sum16(sabs), sd = sum16(gd * gd);
-    if ((tid & 15) == 0 && bl < nb) {
-      ctl.scal[bl][m][0] = sg;
-      ctl.scal[bl][m][1] = sa;
-      ctl.scal[bl][m][2] = sd;
-    }
-  }
-}
-
-// After A(r): the CTA's sums of every (sample, modality, quantity) of the round, as
-// epoch-tagged words. The per-warp partials are added in a fixed order.
-__device__ void publish(const ObjectiveArgs& a, SmemCtl& ctl, int r, int cta, int G) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int b0 = r * a.spr;
-  const int nb = round_size(a, r);
-  const int rows = nb * a.M * kQuantities;
-  for (int u = warp; u < rows; u += kWarps) {
-    const int bl = u / (a.M * kQuantities);
-    const int m = (u / kQuantities) % a.M;
-    const int q = u % kQuantities;
-    float s = lane < kWarps ? ctl.red[lane][bl][m][q] : 0.f;
-    s = warp_sum(s);
-    if (lane == 0) {
-      if (cta == G - 1) s += ctl.scal[bl][m][q];
-      if ((uint32_t)cta != ctl.withhold)
-        st_word(a.partials + (((int64_t)(b0 + bl) * a.M + m) * kQuantities + q) * a.gmax + cta,
-                pack_word(s, ctl.epoch));
-    }
-  }
-}
-
-// Merge(r): wait (bounded) until every CTA's words of round r carry this call's epoch,
-// add them in CTA order, and derive the per-(sample, modality) gradient factors. A
-// warp reads the words of up to kRowsPerPass rows at once, so one round trip to L2
-// serves all of them.
-constexpr int kRowsPerPass = 3;
-constexpr int kWordsPerLane = 5;   // CTAs 32 j + lane, j < 5: 160 CTAs per pass
-
-template <typename T, int MODE>
-__device__ bool merge(const ObjectiveArgs& a, SmemCtl& ctl, int r, int G) {
-  using Tr = Traits<T, MODE>;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int ci = r & 1;
-  const int b0 = r * a.spr;
-  const int nb = round_size(a, r);
-  const int rows = nb * a.M * kQuantities;
-  const uint32_t E = ctl.epoch;
-  const float qnan = __int_as_float(0x7fc00000);
-  for (int u0 = warp; u0 < rows; u0 += kWarps * kRowsPerPass) {
-    float s[kRowsPerPass];
-#pragma unroll
-    for (int i = 0; i < kRowsPerPass; ++i) s[i] = 0.f;
-    for (int base = 0; base < G; base += 32 * kWordsPerLane) {
-      uint64_t w[kRowsPerPass][kWordsPerLane];
-      uint64_t start = 0;
-      for (;;) {
-        bool ready = true;
-#pragma unroll
-        for (int i = 0; i < kRowsPerPass; ++i) {
-          const int u = u0 + i * kWarps;
-          const uint64_t* src = a.partials + ((int64_t)b0 * a.M * kQuantities + u) * a.gmax;
-#pragma unroll
-          for (int j = 0; j < kWordsPerLane; ++j) {
-            const int c = base + lane + 32 * j;
-            w[i][j] = (u < rows && c < G) ? ld_word(src + c) : pack_word(0.f, E);
-            ready &= (uint32_t)(w[i][j] >> 32) == E;
-          }
-        }
-        if (__all_sync(0xffffffffu, ready)) break;
-        const uint64_t now = global_timer_ns();
-        if (start == 0) start = now;
-        if (now - start > ctl.timeout_ns || *reinterpret_cast<volatile int*>(&ctl.abort)) {
-          if (lane == 0 && !*reinterpret_cast<volatile int*>(&ctl.abort)) {
-            ctl.abort = 1;
-            atomicOr(a.status, T2VA_STATUS_TIMEOUT);
-            atomicExch(&a.hdr->poisoned, 1u);
-          }
-          break;
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kRowsPerPass; ++i)
-#pragma unroll
-        for (int j = 0; j < kWordsPerLane; ++j) s[i] += __uint_as_float((uint32_t)w[i][j]);
-    }
-#pragma unroll
-    for (int i = 0; i < kRowsPerPass; ++i) {
-      const int u = u0 + i * kWarps;
-      const float tot = warp_sum(s[i]);
-      if (lane == 0 && u < rows) {
-        const int bl = u / (a.M * kQuantities);
-        const int m = (u / kQuantities) % a.M;
-        const int q = u % kQuantities;
-        ctl.tot[ci][bl][m][q] = tot;
-        const RoundCoef& k = ctl.coef[ci][bl];
-        if (Tr::kScm && q == 0) {
-          const float n = sqrtf(tot);
-          ctl.scaleS[ci][bl][m] = 2.f * a.lam_s * a.w[m] / (k.s * (n + a.eps_s));
-        }
-        if (Tr::kDmd && q == 1) {
-          const float c = a.n[m] > 0 ? tot / (float)a.n[m] : 0.f;
-          ctl.scaleD[ci][bl][m] = k.ok ? 2.f * a.lam_d * a.w[m] / (c + a.eps_d) : qnan;
-        }
-      }
-    }
-  }
-  __syncthreads();
-  return !ctl.abort;
-}
-
-// ---------------------------------------------------------------------------
-// gradients
-// ---------------------------------------------------------------------------
-
 // Eight consecutive gradients (32 bytes, 32-byte aligned) in one store, so every
 // store instruction of a warp writes whole 32-byte sectors.
 __device__ __forceinline__ void write8(float* dst, const float* v, int accumulate) {
@@ -454,13 +243,25 @@ __device__ __forceinline__ void write8(float* dst, const float* v, int accumulat
                : "memory");
 }
 
-__device__ __forceinline__ void write4(float* dst, float4 o, int accumulate) {
-  float4* d = reinterpret_cast<float4*>(dst);
+__device__ __forceinline__ void write4(float* dst, const float* v, int accumulate) {
+  float4 o = make_float4(v[0], v[1], v[2], v[3]);
   if (accumulate) {
-    const float4 old = *d;
+    const float4 old = *reinterpret_cast<const float4*>(dst);
     o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
   }
-  st_stream16(d, o);
+  st_stream16(dst, o);
+}
+
+template <int VE>
+__device__ __forceinline__ void write_run(float* dst, const float* v, bool wide, int accumulate) {
+  if constexpr (VE == 8) {
+    if (wide) {
+      write8(dst, v, accumulate);
+      return;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < VE; i += 4) write4(dst + i, v + i, accumulate);
 }
 
 template <typename T, int MODE>
@@ -468,46 +269,23 @@ __device__ __forceinline__ void write_vec(const ObjectiveArgs& a, int m, int64_t
                                           float scD, const float* gs, const float* gd) {
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
-  const bool alias = Tr::kScm && Tr::kDmd && ((a.alias_mask >> m) & 1u);
-  if constexpr (VE == 8) {
-    if ((a.wide_mask >> m) & 1u) {  // both gradient buffers of m are 32-byte aligned
-      float o[8];
-      if (alias) {
+  const bool wide = (a.wide_mask >> m) & 1u;
+  float o[VE];
+  if (Tr::kScm && Tr::kDmd && ((a.alias_mask >> m) & 1u)) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = scS * gs[i] + scD * gd[i];
-        write8(a.grad_s[m] + e, o, a.accumulate);
-        return;
-      }
-      if constexpr (Tr::kScm) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = scS * gs[i];
-        write8(a.grad_s[m] + e, o, a.accumulate);
-      }
-      if constexpr (Tr::kDmd) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = scD * gd[i];
-        write8(a.grad_d[m] + e, o, a.accumulate);
-      }
-      return;
-    }
+    for (int i = 0; i < VE; ++i) o[i] = scS * gs[i] + scD * gd[i];
+    write_run<VE>(a.grad_s[m] + e, o, wide, a.accumulate);
+    return;
   }
+  if constexpr (Tr::kScm) {
 #pragma unroll
-  for (int i = 0; i < VE; i += 4) {
-    if (alias) {
-      write4(a.grad_s[m] + e + i,
-             make_float4(scS * gs[i] + scD * gd[i], scS * gs[i + 1] + scD * gd[i + 1],
-                         scS * gs[i + 2] + scD * gd[i + 2], scS * gs[i + 3] + scD * gd[i + 3]),
-             a.accumulate);
-    } else {
-      if constexpr (Tr::kScm)
-        write4(a.grad_s[m] + e + i,
-               make_float4(scS * gs[i], scS * gs[i + 1], scS * gs[i + 2], scS * gs[i + 3]),
-               a.accumulate);
-      if constexpr (Tr::kDmd)
-        write4(a.grad_d[m] + e + i,
-               make_float4(scD * gd[i], scD * gd[i + 1], scD * gd[i + 2], scD * gd[i + 3]),
-               a.accumulate);
-    }
+    for (int i = 0; i < VE; ++i) o[i] = scS * gs[i];
+    write_run<VE>(a.grad_s[m] + e, o, wide, a.accumulate);
+  }
+  if constexpr (Tr::kDmd) {
+#pragma unroll
+    for (int i = 0; i < VE; ++i) o[i] = scD * gd[i];
+    write_run<VE>(a.grad_d[m] + e, o, wide, a.accumulate);
   }
 }
 
@@ -516,223 +294,166 @@ __device__ __forceinline__ void write1(float* dst, float v, int accumulate) {
   *dst = v;
 }
 
-// W(r): the gradients of round r and its per-sample outputs.
+// ---------------------------------------------------------------------------
+// pass 1: partial sums per chunk
+// ---------------------------------------------------------------------------
+
 template <typename T, int MODE>
-__device__ void write_round(const ObjectiveArgs& a, SmemCtl& ctl, const float4* group, int r,
-                            int cta, int G) {
+__global__ void __launch_bounds__(kThreads, 3) k_sums(const __grid_constant__ ObjectiveArgs a) {
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
-  const int tid = threadIdx.x;
-  const int ci = r & 1;
-  const int b0 = r * a.spr;
-  const int nb = round_size(a, r);
-  const int64_t kstride = (int64_t)a.spr * a.keep_f;
-  const float qnan = __int_as_float(0x7fc00000);
-
-  if (tid < a.sample_f) {
-    for (int bl = 0; bl < nb; ++bl) {
-      for (int slot = tid; slot < a.sample_f; slot += kThreads) {
-        const Item it{r, bl, slot};
-        const Where w = locate<VE>(it, cta, a);
-        if (!w.valid) continue;
+  __shared__ float3 scratch[kWarps];
+  const Chunk k = chunk_of<VE>(a, blockIdx.x);
+  const Coefs cf = coefs_of<T, MODE>(a, k.b);
+  const uint64_t keep = policy_evict_last();
+  float sg = 0.f, sa = 0.f, sd = 0.f;
+  for (int64_t base = k.v_lo; base < k.v_hi; base += kBatchVec) {
+    uint4 in[kPerThread][Tr::NIN];
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {  // every load of the batch first
+      const int64_t v = base + u * kThreads + threadIdx.x;
+      if (v < k.v_hi) load_vec<T, MODE>(in[u], a, k.m, k.e_vec0 + v * VE, keep);
+    }
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+      const int64_t v = base + u * kThreads + threadIdx.x;
+      if (v < k.v_hi) {
         float gs[VE], gd[VE];
-        if (slot < a.keep_f) {
-          fetch<T, MODE>(group, kstride, (int64_t)bl * a.keep_f + slot, gs, gd);
-        } else {  // not kept on chip: recompute from the inputs
-          Loaded<T, MODE> L;
-          load_vec<T, MODE>(L, a, w.m, w.e);
-          float d0 = 0.f, d1 = 0.f, d2 = 0.f;
-          directions<T, MODE>(L, ctl.coef[ci][bl], gs, gd, d0, d1, d2);
-        }
-        const float scS = Tr::kScm ? ctl.scaleS[ci][bl][w.m] : 0.f;
-        const float scD = Tr::kDmd ? ctl.scaleD[ci][bl][w.m] : 0.f;
-        write_vec<T, MODE>(a, w.m, w.e, scS, scD, gs, gd);
+        directions<T, MODE>(in[u], cf, gs, gd, sg, sa, sd);
       }
     }
   }
-
-  // unaligned head/tail elements (CTA G-1)
-  if (cta == G - 1) {
-    int bl, m;
-    const int64_t e = scalar_element<VE>(a, b0, nb, bl, m);
-    if (e >= 0) {
-      float gs = 0.f, gd = 0.f, sabs = 0.f;
-      scalar_direction<T, MODE>(a, m, e, ctl.coef[ci][bl], gs, gd, sabs);
-      const float scS = Tr::kScm ? ctl.scaleS[ci][bl][m] : 0.f;
-      const float scD = Tr::kDmd ? ctl.scaleD[ci][bl][m] : 0.f;
-      if (Tr::kScm && Tr::kDmd && ((a.alias_mask >> m) & 1u)) {
-        write1(a.grad_s[m] + e, scS * gs + scD * gd, a.accumulate);
-      } else {
-        if constexpr (Tr::kScm) write1(a.grad_s[m] + e, scS * gs, a.accumulate);
-        if constexpr (Tr::kDmd) write1(a.grad_d[m] + e, scD * gd, a.accumulate);
-      }
-    }
+  const int64_t e = edge_element<VE>(a, k);
+  if (e >= 0) {
+    float gs = 0.f, gd = 0.f, sabs = 0.f;
+    scalar_direction<T, MODE>(a, k.m, e, cf, gs, gd, sabs);
+    sg = fmaf(gs, gs, sg);
+    sa += sabs;
+    sd = fmaf(gd, gd, sd);
   }
-
-  // per-sample outputs: sample b is written by CTA b % G
-  for (int bl = tid; bl < nb; bl += kThreads) {
-    const int b = b0 + bl;
-    if (b % G != cta) continue;
-    const RoundCoef& k = ctl.coef[ci][bl];
-    float Ls = 0.f, Ld = 0.f;
-    for (int m = 0; m < a.M; ++m) {
-      if constexpr (Tr::kScm) {
-        const float Sg = ctl.tot[ci][bl][m][0];
-        const float n = sqrtf(Sg);
-        const float d = n + a.eps_s;
-        Ls += a.w[m] * (Sg / (d * d));
-        if (a.norm) a.norm[(int64_t)b * a.M + m] = k.ok ? n : qnan;
-      }
-      if constexpr (Tr::kDmd) {
-        const float c = a.n[m] > 0 ? ctl.tot[ci][bl][m][1] / (float)a.n[m] : 0.f;
-        const float d = c + a.eps_d;
-        Ld += a.w[m] * (ctl.tot[ci][bl][m][2] / (d * d));
-        if (a.cdmd) a.cdmd[(int64_t)b * a.M + m] = k.ok ? c : qnan;
-      }
-    }
-    Ls *= a.lam_s;
-    Ld *= a.lam_d;
-    if (!k.ok) {
-      Ls = qnan;
-      Ld = qnan;
-      atomicOr(a.status, T2VA_STATUS_BAD_TIMESTEP);
-    }
-    a.loss[b] = (Tr::kScm ? Ls : 0.f) + (Tr::kDmd ? Ld : 0.f);
-    if (a.loss_s) a.loss_s[b] = Ls;
-    if (a.loss_d) a.loss_d[b] = Ld;
-  }
+  const float3 t = block_sum3(sg, sa, sd, scratch);
+  if (threadIdx.x == 0) row_partials(a, k.b, k.m)[k.c] = make_float4(t.x, t.y, t.z, 0.f);
 }
 
 // ---------------------------------------------------------------------------
-// the kernel
+// pass 2: totals, gradients, per-sample outputs
 // ---------------------------------------------------------------------------
 
+// Totals of row (b, m): the chunks' partial sums added in a fixed order (thread t
+// takes chunks t, t + 256, ...; then lanes; then warps), so every CTA of the row
+// gets the same bits.
+__device__ __forceinline__ float3 row_totals(const ObjectiveArgs& a, int b, int m,
+                                             float3 (&scratch)[kWarps]) {
+  const float4* p = row_partials(a, b, m);
+  float x = 0.f, y = 0.f, z = 0.f;
+  for (int c = threadIdx.x; c < a.nchunk[m]; c += kThreads) {
+    const float4 v = __ldcg(p + c);
+    x += v.x;
+    y += v.y;
+    z += v.z;
+  }
+  return block_sum3(x, y, z, scratch);
+}
+
 template <typename T, int MODE>
-__global__ void __launch_bounds__(kThreads, 1) k_objective(const __grid_constant__ ObjectiveArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) k_grads(const __grid_constant__ ObjectiveArgs a) {
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(smem_raw);
-  float4* kept = reinterpret_cast<float4*>(smem_raw + kCtlBytes);
-  const int64_t kstride = (int64_t)a.spr * a.keep_f;  // float4 per piece of one group
-  const int64_t group_f4 = (int64_t)Tr::kPieces * kstride;
-  const int G = gridDim.x, cta = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ float3 scratch[kWarps];
+  const Chunk k = chunk_of<VE>(a, blockIdx.x);
+  const Coefs cf = coefs_of<T, MODE>(a, k.b);
+  const uint64_t drop = policy_evict_first();
+  const float qnan = __int_as_float(0x7fc00000);
 
-  if (tid == 0) {
-    const uint32_t magic = ld_relaxed_gpu(&a.hdr->magic);
-    const uint32_t poisoned = ld_relaxed_gpu(&a.hdr->poisoned);
-    ctl.timeout_ns = *reinterpret_cast<volatile uint64_t*>(&a.hdr->timeout_ns);
-    ctl.epoch = ld_relaxed_gpu(&a.hdr->epoch);
-    ctl.withhold = ld_relaxed_gpu(&a.hdr->withhold_cta);
-    ctl.abort = 0;
-    if (magic != kWsMagic || poisoned != 0 || ctl.epoch == 0) {
-      ctl.abort = 1;
-      atomicOr(a.status, T2VA_STATUS_BAD_WORKSPACE);
+  // the first batch's loads (served by L2) are in flight while the totals are read
+  uint4 in[kPerThread][Tr::NIN];
+  int64_t base = k.v_lo;
+#pragma unroll
+  for (int u = 0; u < kPerThread; ++u) {
+    const int64_t v = base + u * kThreads + threadIdx.x;
+    if (v < k.v_hi) load_vec<T, MODE>(in[u], a, k.m, k.e_vec0 + v * VE, drop);
+  }
+
+  const float3 tot = row_totals(a, k.b, k.m, scratch);
+  const float n = sqrtf(tot.x);
+  const float scS = Tr::kScm ? 2.f * a.lam_s * a.w[k.m] / (cf.s * (n + a.eps_s)) : 0.f;
+  const float c_dmd = a.n[k.m] > 0 ? tot.y / (float)a.n[k.m] : 0.f;
+  const float scD = Tr::kDmd ? (cf.ok ? 2.f * a.lam_d * a.w[k.m] / (c_dmd + a.eps_d) : qnan) : 0.f;
+
+  for (;;) {
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+      const int64_t v = base + u * kThreads + threadIdx.x;
+      if (v < k.v_hi) {
+        float gs[VE], gd[VE], d0 = 0.f, d1 = 0.f, d2 = 0.f;
+        directions<T, MODE>(in[u], cf, gs, gd, d0, d1, d2);
+        write_vec<T, MODE>(a, k.m, k.e_vec0 + v * VE, scS, scD, gs, gd);
+      }
+    }
+    base += kBatchVec;
+    if (base >= k.v_hi) break;
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+      const int64_t v = base + u * kThreads + threadIdx.x;
+      if (v < k.v_hi) load_vec<T, MODE>(in[u], a, k.m, k.e_vec0 + v * VE, drop);
     }
   }
-  for (int u = lane; u < kMaxRound * kMaxM * kQuantities; u += 32)
-    (&ctl.red[warp][0][0][0])[u] = 0.f;
-  __syncthreads();
-  if (ctl.abort) return;
 
-  // the first slot's loads
-  Item it;
-  bool have = item_begin(it, 0, a);
-  Loaded<T, MODE> Lc;
-  Where wc{0, 0, false};
-  if (have) {
-    wc = locate<VE>(it, cta, a);
-    if (wc.valid) load_vec<T, MODE>(Lc, a, wc.m, wc.e);
+  const int64_t e = edge_element<VE>(a, k);
+  if (e >= 0) {
+    float gs = 0.f, gd = 0.f, sabs = 0.f;
+    scalar_direction<T, MODE>(a, k.m, e, cf, gs, gd, sabs);
+    if (Tr::kScm && Tr::kDmd && ((a.alias_mask >> k.m) & 1u)) {
+      write1(a.grad_s[k.m] + e, scS * gs + scD * gd, a.accumulate);
+    } else {
+      if constexpr (Tr::kScm) write1(a.grad_s[k.m] + e, scS * gs, a.accumulate);
+      if constexpr (Tr::kDmd) write1(a.grad_d[k.m] + e, scD * gd, a.accumulate);
+    }
   }
 
-  for (int r = 0; r < a.rounds; ++r) {
-    const int ci = r & 1;
-    __syncthreads();  // the previous round's W (and reads of its group) are done
-    round_setup<T, MODE>(a, ctl, r, cta, G);
-    __syncthreads();
-    float4* group = kept + (r % a.groups) * group_f4;
-
-    // A(r): the next slot's loads are in flight while this one is computed
-    float sg = 0.f, sa = 0.f, sd = 0.f;
-    while (have && it.r == r) {
-      Item nx = it;
-      const bool have_n = item_next(nx, a);
-      Loaded<T, MODE> Ln;
-      Where wn{0, 0, false};
-      if (have_n) {
-        wn = locate<VE>(nx, cta, a);
-        if (wn.valid) load_vec<T, MODE>(Ln, a, wn.m, wn.e);
-      }
-      if (wc.valid) {
-        float gs[VE], gd[VE];
-        directions<T, MODE>(Lc, ctl.coef[ci][it.bl], gs, gd, sg, sa, sd);
-        if (it.slot < a.keep_f)
-          keep<T, MODE>(group, kstride, (int64_t)it.bl * a.keep_f + it.slot, gs, gd);
-      }
-      // a warp's slots change (sample, modality) together: flush its sums then
-      if (!have_n || nx.r != r || nx.bl != it.bl || wn.m != wc.m) {
-        sg = warp_sum(sg);
-        sa = warp_sum(sa);
-        sd = warp_sum(sd);
-        if (lane == 0) {
-          ctl.red[warp][it.bl][wc.m][0] += sg;
-          ctl.red[warp][it.bl][wc.m][1] += sa;
-          ctl.red[warp][it.bl][wc.m][2] += sd;
+  // per-sample outputs: by the first chunk of the sample's first modality, from the
+  // totals of all its modalities (added in the same order as everywhere else)
+  if (k.m == 0 && k.c == 0) {
+    float Ls = 0.f, Ld = 0.f;
+    for (int m = 0; m < a.M; ++m) {
+      const float3 tm = m == 0 ? tot : row_totals(a, k.b, m, scratch);
+      if (threadIdx.x == 0) {
+        if constexpr (Tr::kScm) {
+          const float nm = sqrtf(tm.x);
+          const float d = nm + a.eps_s;
+          Ls += a.w[m] * (tm.x / (d * d));
+          if (a.norm) a.norm[(int64_t)k.b * a.M + m] = cf.ok ? nm : qnan;
         }
-        sg = sa = sd = 0.f;
+        if constexpr (Tr::kDmd) {
+          const float c = a.n[m] > 0 ? tm.y / (float)a.n[m] : 0.f;
+          const float d = c + a.eps_d;
+          Ld += a.w[m] * (tm.z / (d * d));
+          if (a.cdmd) a.cdmd[(int64_t)k.b * a.M + m] = cf.ok ? c : qnan;
+        }
       }
-      it = nx;
-      Lc = Ln;
-      wc = wn;
-      have = have_n;
     }
-    __syncthreads();  // per-warp sums and head/tail sums complete
-    publish(a, ctl, r, cta, G);
-    __syncthreads();  // sums read: clear this warp's rows for the next round
-    for (int u = lane; u < kMaxRound * kMaxM * kQuantities; u += 32)
-      (&ctl.red[warp][0][0][0])[u] = 0.f;
-
-    if (a.groups == 1) {
-      if (!merge<T, MODE>(a, ctl, r, G)) return;
-      write_round<T, MODE>(a, ctl, group, r, cta, G);
-    } else if (r >= 1) {
-      if (!merge<T, MODE>(a, ctl, r - 1, G)) return;
-      write_round<T, MODE>(a, ctl, kept + ((r - 1) % a.groups) * group_f4, r - 1, cta, G);
+    if (threadIdx.x == 0) {
+      Ls *= a.lam_s;
+      Ld *= a.lam_d;
+      if (!cf.ok) {
+        Ls = qnan;
+        Ld = qnan;
+        atomicOr(a.status, T2VA_STATUS_BAD_TIMESTEP);
+      }
+      a.loss[k.b] = (Tr::kScm ? Ls : 0.f) + (Tr::kDmd ? Ld : 0.f);
+      if (a.loss_s) a.loss_s[k.b] = Ls;
+      if (a.loss_d) a.loss_d[k.b] = Ld;
     }
-  }
-  if (a.groups > 1 && a.rounds > 0) {
-    const int r = a.rounds - 1;
-    if (!merge<T, MODE>(a, ctl, r, G)) return;
-    write_round<T, MODE>(a, ctl, kept + (r % a.groups) * group_f4, r, cta, G);
-  }
-  // Every CTA has published its last round's words, tagged with this epoch, before
-  // CTA 0's last merge could finish: all of them have read the epoch, so it can move
-  // on for the next call.
-  if (cta == 0 && tid == 0) {
-    const uint32_t next = ctl.epoch + 1u;
-    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(&a.hdr->epoch),
-                 "r"(next == 0u ? 1u : next)
-                 : "memory");
   }
 }
 
 template <typename T, int MODE>
 cudaError_t launch_t(const ObjectiveArgs& a, const ObjectiveLaunch& l, cudaStream_t st) {
-  auto kern = k_objective<T, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.smem);
+  k_sums<T, MODE><<<l.grid, kThreads, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(l.grid);
-  cfg.blockDim = dim3(l.threads);
-  cfg.dynamicSmemBytes = l.smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // every CTA is resident: the waits always end
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  k_grads<T, MODE><<<l.grid, kThreads, 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 __global__ void k_ws_init(uint4* ws, size_t n16, uint64_t timeout_ns, uint32_t gmax) {
@@ -745,9 +466,6 @@ __global__ void k_ws_init(uint4* ws, size_t n16, uint64_t timeout_ns, uint32_t g
     WsHeader* h = reinterpret_cast<WsHeader*>(ws);
     h->timeout_ns = timeout_ns;
     h->gmax = gmax;
-    h->poisoned = 0;
-    h->epoch = 1;  // zeroed words carry epoch 0, so no word of a fresh workspace is final
-    h->withhold_cta = kNoWithhold;
     __threadfence();
     h->magic = kWsMagic;
   }
@@ -755,53 +473,31 @@ __global__ void k_ws_init(uint4* ws, size_t n16, uint64_t timeout_ns, uint32_t g
 
 }  // namespace
 
-bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int mode, int sm_count, size_t smem_optin,
-                    size_t /*l2_bytes*/, ObjectiveLaunch* out) {
+bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int /*mode*/, int /*sm_count*/,
+                    size_t /*smem_optin*/, size_t /*l2_bytes*/, ObjectiveLaunch* out) {
   const int VE = dt == T2VA_BFLOAT16 ? 8 : 4;
-  const int Q = ((mode & kModeScm) ? 1 : 0) + ((mode & kModeDmd) ? 1 : 0);
-  const int64_t slot_bytes = (int64_t)Q * VE / 4 * 16;  // kept direction bytes per slot
-  int64_t vtot = 0, nvec_ub[kMaxM];
+  // vectors per chunk: one batch of the CTA, more if a row would need more chunks
+  // than the workspace holds
+  int64_t nvec_max = 0;
+  for (int m = 0; m < a.M; ++m) nvec_max = std::max<int64_t>(nvec_max, (a.n[m] + VE - 1) / VE);
+  const int64_t batches = std::max<int64_t>(1, (nvec_max + (int64_t)kBatchVec * kMaxChunks - 1) /
+                                                   ((int64_t)kBatchVec * kMaxChunks));
+  if (batches > INT32_MAX / kBatchVec) return false;
+  a.vpc = (int)(batches * kBatchVec);
+  int acc = 0;
   for (int m = 0; m < a.M; ++m) {
-    nvec_ub[m] = (a.n[m] + VE - 1) / VE;
-    vtot += nvec_ub[m];
+    const int64_t nvec_ub = (a.n[m] + VE - 1) / VE;
+    const int64_t c = std::max<int64_t>(1, (nvec_ub + a.vpc - 1) / a.vpc);  // >= 1: edges
+    a.nchunk[m] = (int)c;
+    a.choff[m] = acc;
+    acc += (int)c;
   }
-  int64_t G = (vtot + kThreads - 1) / kThreads;  // small problems use fewer CTAs
-  G = std::max<int64_t>(1, std::min<int64_t>({G, (int64_t)sm_count, (int64_t)a.gmax}));
-  int64_t acc = 0;
-  for (int m = 0; m < a.M; ++m) {
-    a.chunk[m] = (nvec_ub[m] + G - 1) / G;
-    a.choff[m] = (int)std::min<int64_t>(acc, INT32_MAX);
-    acc += (a.chunk[m] + 31) / 32 * 32;
-    if (acc > (int64_t)1 << 30) return false;
-  }
-  for (int m = a.M; m < kMaxM; ++m) {
-    a.chunk[m] = 0;
-    a.choff[m] = (int)acc;
-  }
-  a.sample_f = (int)acc;
-  if (smem_optin <= kCtlBytes + (size_t)32 * slot_bytes) return false;
-  const int64_t budget = (int64_t)(smem_optin - kCtlBytes);
-  const int64_t per_sample = a.sample_f * slot_bytes;
-  a.keep_f = a.sample_f;
-  if (per_sample == 0 || (a.B <= kMaxRound && a.B * per_sample <= budget)) {
-    a.groups = 1;  // one round: A, merge, W
-    a.spr = std::max(1, std::min(a.B, kMaxRound));
-  } else if (a.B >= 2 && 2 * per_sample <= budget) {
-    a.groups = 2;  // A0 A1 W0 A2 W1 ...
-    const int64_t spr = std::min<int64_t>({budget / (2 * per_sample), (a.B + 1) / 2, kMaxRound});
-    a.spr = (int)std::max<int64_t>(1, spr);
-  } else if (per_sample <= budget) {
-    a.groups = 1;
-    a.spr = 1;
-  } else {  // one sample's directions exceed shared memory: keep a prefix of its slots
-    a.groups = 1;
-    a.spr = 1;
-    a.keep_f = (int)(budget / slot_bytes / 32 * 32);
-  }
-  a.rounds = (a.B + a.spr - 1) / a.spr;
-  out->grid = (int)G;
+  for (int m = a.M; m <= kMaxM; ++m) a.choff[m] = acc;
+  const int64_t grid = (int64_t)a.B * acc;
+  if (grid > INT32_MAX) return false;
+  out->grid = (int)grid;
   out->threads = kThreads;
-  out->smem = kCtlBytes + (size_t)a.groups * a.spr * a.keep_f * slot_bytes;
+  out->smem = 0;
   return true;
 }
 

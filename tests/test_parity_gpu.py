@@ -289,36 +289,29 @@ def test_cuda_graph_capture_matches_eager():
 
 
 # --------------------------------------------------------------------------
-# failure detection: bounded waits, workspace checks (no fault, no hang)
+# the workspace: per-chunk partial sums written and read within one call
 # --------------------------------------------------------------------------
 
-def test_timeout_sets_status_and_poisons_workspace():
-    """The workspace header's withhold field (32-bit word 6 of the header) names a CTA
-    that publishes no partial sums, so no CTA ever sees all of them: every wait gives
-    up after the workspace's limit (200 ms here), sets TIMEOUT and returns. The
-    workspace then refuses work until it is initialised again (which also clears the
-    field)."""
-    inp = S.make_inputs(2, [50000, 500], "bf16", S.STAGE3, seed=(400,))
-    p = Params()
-    ws = t2va.new_workspace(2, 2, timeout_ms=200)
-    torch.cuda.synchronize()
-    ws.view(torch.int32)[6] = 0   # CTA 0 withholds its sums
-    bad = gpu_run(inp, p, S.STAGE3, workspace=ws)
-    assert bad["status"] & t2va.STATUS_TIMEOUT
+def test_workspace_contents_do_not_matter():
+    """The first kernel of a call writes every partial sum the second one reads, so a
+    workspace full of garbage (never initialised, or left by a call with other sizes)
+    gives bit-identical results."""
+    inp = S.make_inputs(3, [50_003, 701], "bf16", S.STAGE3, seed=(400,))
+    p = Params(weight=(1.0, 3.0))
+    clean = gpu_run(inp, p, S.STAGE3)
+    ws = torch.randint(0, 256, (t2va.workspace_bytes(3, 2),), dtype=torch.uint8, device="cuda")
+    dirty = gpu_run(inp, p, S.STAGE3, workspace=ws)
+    assert dirty["status"] == 0
+    for k in ("loss", "norm", "cdmd"):
+        assert np.array_equal(clean[k], dirty[k])
+    for k in ("grad_x0_student", "grad_zhat0"):
+        for x, y in zip(clean[k], dirty[k]):
+            assert np.array_equal(x, y)
+    # the same workspace for a call with other sizes, then this call again
+    other = S.make_inputs(2, [777, 33], "bf16", S.STAGE3, seed=(401,))
+    gpu_run(other, p, S.STAGE3, workspace=ws)
     again = gpu_run(inp, p, S.STAGE3, workspace=ws)
-    assert again["status"] & t2va.STATUS_BAD_WORKSPACE
-    t2va.workspace_init(ws, 200)
-    good = gpu_run(inp, p, S.STAGE3, workspace=ws)
-    assert good["status"] == 0
-    compare(good, oracle_run(inp, p, S.STAGE3), "bf16", S.STAGE3)
-
-
-def test_uninitialised_workspace_is_refused():
-    inp = S.make_inputs(2, [5000, 50], "bf16", S.STAGE3, seed=(401,))
-    ws = torch.zeros(t2va.workspace_bytes(2, 2), dtype=torch.uint8, device="cuda")
-    out = gpu_run(inp, Params(), S.STAGE3, workspace=ws)
-    assert out["status"] & t2va.STATUS_BAD_WORKSPACE
-    assert np.all(np.isnan(out["loss"]))   # nothing was written
+    assert np.array_equal(clean["loss"], again["loss"])
 
 
 def test_host_errors_on_device():
