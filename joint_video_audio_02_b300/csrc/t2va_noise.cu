@@ -66,6 +66,10 @@ __global__ void __launch_bounds__(kNoiseThreads) k_noise(const __grid_constant__
   const int b = local / a.chunks[m];
   const int chunk = local - b * a.chunks[m];
 
+  // launched as a programmatic dependent of the previous kernel on the stream: no
+  // memory access before that kernel has finished
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const float t = __ldg(a.t + b);
   float s, c;
   sincosf(t, &s, &c);
@@ -117,19 +121,18 @@ __global__ void __launch_bounds__(kNoiseThreads) k_noise(const __grid_constant__
 int noise_vectors_per_cta() { return kNoiseVecPerCta; }
 
 cudaError_t launch_noise(const NoiseArgs& a, t2va_dtype dt, int grid, cudaStream_t st) {
-  // The kernel uses no shared memory; asking for the largest shared-memory carveout
-  // anyway lets the objective kernel that usually follows (which needs most of it)
-  // start without reconfiguring the SMs.
-  if (dt == T2VA_BFLOAT16) {
-    cudaFuncSetAttribute(k_noise<__nv_bfloat16>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
-    k_noise<__nv_bfloat16><<<grid, kNoiseThreads, 0, st>>>(a);
-  } else {
-    cudaFuncSetAttribute(k_noise<float>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
-    k_noise<float><<<grid, kNoiseThreads, 0, st>>>(a);
-  }
-  return cudaGetLastError();
+  // a programmatic dependent of the previous work on the stream (see k_noise)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kNoiseThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (dt == T2VA_BFLOAT16) return cudaLaunchKernelEx(&cfg, k_noise<__nv_bfloat16>, a);
+  return cudaLaunchKernelEx(&cfg, k_noise<float>, a);
 }
 
 }  // namespace t2va

@@ -303,6 +303,11 @@ __global__ void __launch_bounds__(kThreads, 3) k_sums(const __grid_constant__ Ob
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
   __shared__ float3 scratch[kWarps];
+  // launched as a programmatic dependent of the previous kernel on the stream: no
+  // memory access before that kernel has finished; the next kernel (k_grads) may
+  // launch once every CTA of this one is past this point
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const Chunk k = chunk_of<VE>(a, blockIdx.x);
   const Coefs cf = coefs_of<T, MODE>(a, k.b);
   const uint64_t keep = policy_evict_last();
@@ -374,6 +379,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_grads(const __grid_constant__ O
     if (v < k.v_hi) load_vec<T, MODE>(in[u], a, k.m, k.e_vec0 + v * VE, drop);
   }
 
+  // The inputs were complete before k_sums read them (every CTA of k_sums waited for
+  // its predecessor before this kernel could launch), so the loads above may run
+  // ahead; the partial sums of k_sums may not be read before it has finished.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const float3 tot = row_totals(a, k.b, k.m, scratch);
   const float n = sqrtf(tot.x);
   const float scS = Tr::kScm ? 2.f * a.lam_s * a.w[k.m] / (cf.s * (n + a.eps_s)) : 0.f;
@@ -447,13 +457,28 @@ __global__ void __launch_bounds__(kThreads, 2) k_grads(const __grid_constant__ O
   }
 }
 
+// Launch as a programmatic dependent of the previous work on the stream: the kernel
+// may be scheduled while that work drains, and waits for it (griddepcontrol.wait)
+// before touching memory that work could have written.
+template <typename K>
+cudaError_t launch_pdl(K kern, int grid, cudaStream_t st, const ObjectiveArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
 template <typename T, int MODE>
 cudaError_t launch_t(const ObjectiveArgs& a, const ObjectiveLaunch& l, cudaStream_t st) {
-  k_sums<T, MODE><<<l.grid, kThreads, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(k_sums<T, MODE>, l.grid, st, a);
   if (e != cudaSuccess) return e;
-  k_grads<T, MODE><<<l.grid, kThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_grads<T, MODE>, l.grid, st, a);
 }
 
 __global__ void k_ws_init(uint4* ws, size_t n16, uint64_t timeout_ns, uint32_t gmax) {
