@@ -14,8 +14,8 @@
 //             and sum g_DMD^2; the CTA adds them in a fixed order and writes the
 //             chunk's three partial sums to the workspace. The loads ask L2 to keep
 //             the inputs.
-//   k_grads : the same chunks. Each CTA starts the loads of its vectors again (L2
-//             hits; L2 may drop them now), adds the row's partial sums in chunk order
+//   k_grads : the same chunks. Each CTA starts the loads of its vectors again, except
+//             zhat0 (L2 hits; L2 may drop them now), adds the row's partial sums in chunk order
 //             (every CTA of a row gets bit-identical totals), derives the gradient
 //             factors, recomputes the directions and writes the float32 gradients
 //             once. The first chunk of each sample also writes the per-sample outputs.
@@ -42,6 +42,9 @@ struct Traits {
   static constexpr bool kDmd = (MODE & kModeDmd) != 0;
   static constexpr int k0 = kScm ? kZt : kZh;  // first input slot of the mode
   static constexpr int NIN = (kScm ? 4 : 0) + (kDmd ? 3 : 0);
+  // the gradient pass needs no zhat0 (it enters only the residual scale)
+  static constexpr int NG = (kScm ? 4 : 0) + (kDmd ? 2 : 0);
+  static constexpr int kYT0 = kScm ? 4 : 0;  // position of y_T among the gradient inputs
 };
 
 // ---------------------------------------------------------------------------
@@ -205,6 +208,46 @@ __device__ __forceinline__ void directions(const uint4 (&in)[Traits<T, MODE>::NI
   }
 }
 
+// The gradient pass's inputs of one vector: the sCM inputs, then y_T and y_fake.
+template <typename T, int MODE>
+__device__ __forceinline__ void load_grad_vec(uint4 (&in)[Traits<T, MODE>::NG], const ObjectiveArgs& a,
+                                              int m, int64_t e, uint64_t policy) {
+  using Tr = Traits<T, MODE>;
+  if constexpr (Tr::kScm) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) in[q] = ld16(reinterpret_cast<const T*>(a.in[kZt + q][m]) + e, policy);
+  }
+  if constexpr (Tr::kDmd) {
+    in[Tr::kYT0] = ld16(reinterpret_cast<const T*>(a.in[kYT][m]) + e, policy);
+    in[Tr::kYT0 + 1] = ld16(reinterpret_cast<const T*>(a.in[kYF][m]) + e, policy);
+  }
+}
+
+// The unscaled directions of one vector from the gradient pass's inputs.
+template <typename T, int MODE>
+__device__ __forceinline__ void grad_directions(const uint4 (&in)[Traits<T, MODE>::NG],
+                                                const Coefs& k, float* gs, float* gd) {
+  using Tr = Traits<T, MODE>;
+  constexpr int VE = Tr::VE;
+  if constexpr (Tr::kScm) {
+    Vec<T> z, xt, xs, xd;
+    z.from(in[0]);
+    xt.from(in[1]);
+    xs.from(in[2]);
+    xd.from(in[3]);
+#pragma unroll
+    for (int i = 0; i < VE; ++i)
+      gs[i] = fmaf(k.kD, xt.v[i] - xs.v[i], fmaf(k.kz, z.v[i], k.kx * xd.v[i]));
+  }
+  if constexpr (Tr::kDmd) {
+    Vec<T> yt, yf;
+    yt.from(in[Tr::kYT0]);
+    yf.from(in[Tr::kYT0 + 1]);
+#pragma unroll
+    for (int i = 0; i < VE; ++i) gd[i] = yf.v[i] - yt.v[i];
+  }
+}
+
 template <typename T, int MODE>
 __device__ __forceinline__ void scalar_direction(const ObjectiveArgs& a, int m, int64_t e,
                                                  const Coefs& k, float& gs, float& gd,
@@ -361,7 +404,7 @@ __device__ __forceinline__ float3 row_totals(const ObjectiveArgs& a, int b, int 
 }
 
 template <typename T, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) k_grads(const __grid_constant__ ObjectiveArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) k_grads(const __grid_constant__ ObjectiveArgs a) {
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
   __shared__ float3 scratch[kWarps];
@@ -371,12 +414,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_grads(const __grid_constant__ O
   const float qnan = __int_as_float(0x7fc00000);
 
   // the first batch's loads (served by L2) are in flight while the totals are read
-  uint4 in[kPerThread][Tr::NIN];
+  uint4 in[kPerThread][Tr::NG];
   int64_t base = k.v_lo;
 #pragma unroll
   for (int u = 0; u < kPerThread; ++u) {
     const int64_t v = base + u * kThreads + threadIdx.x;
-    if (v < k.v_hi) load_vec<T, MODE>(in[u], a, k.m, k.e_vec0 + v * VE, drop);
+    if (v < k.v_hi) load_grad_vec<T, MODE>(in[u], a, k.m, k.e_vec0 + v * VE, drop);
   }
 
   // The inputs were complete before k_sums read them (every CTA of k_sums waited for
@@ -395,8 +438,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_grads(const __grid_constant__ O
     for (int u = 0; u < kPerThread; ++u) {
       const int64_t v = base + u * kThreads + threadIdx.x;
       if (v < k.v_hi) {
-        float gs[VE], gd[VE], d0 = 0.f, d1 = 0.f, d2 = 0.f;
-        directions<T, MODE>(in[u], cf, gs, gd, d0, d1, d2);
+        float gs[VE], gd[VE];
+        grad_directions<T, MODE>(in[u], cf, gs, gd);
         write_vec<T, MODE>(a, k.m, k.e_vec0 + v * VE, scS, scD, gs, gd);
       }
     }
@@ -405,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_grads(const __grid_constant__ O
 #pragma unroll
     for (int u = 0; u < kPerThread; ++u) {
       const int64_t v = base + u * kThreads + threadIdx.x;
-      if (v < k.v_hi) load_vec<T, MODE>(in[u], a, k.m, k.e_vec0 + v * VE, drop);
+      if (v < k.v_hi) load_grad_vec<T, MODE>(in[u], a, k.m, k.e_vec0 + v * VE, drop);
     }
   }
 
