@@ -541,15 +541,25 @@ __global__ void k_ws_init(uint4* ws, size_t n16, uint64_t timeout_ns, uint32_t g
 
 }  // namespace
 
-bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int /*mode*/, int /*sm_count*/,
+bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int /*mode*/, int sm_count,
                     size_t /*smem_optin*/, size_t /*l2_bytes*/, ObjectiveLaunch* out) {
   const int VE = dt == T2VA_BFLOAT16 ? 8 : 4;
-  // vectors per chunk: one batch of the CTA, more if a row would need more chunks
-  // than the workspace holds
-  int64_t nvec_max = 0;
-  for (int m = 0; m < a.M; ++m) nvec_max = std::max<int64_t>(nvec_max, (a.n[m] + VE - 1) / VE);
-  const int64_t batches = std::max<int64_t>(1, (nvec_max + (int64_t)kBatchVec * kMaxChunks - 1) /
-                                                   ((int64_t)kBatchVec * kMaxChunks));
+  // Vectors per chunk: one batch of the CTA, or two when a one-batch grid would need
+  // between one and four waves of resident CTAs (three per SM): the grid then fits in
+  // fewer waves and each CTA's fixed costs are shared by twice the work (measured on
+  // B300: 512x768 batch 4 19.5 -> 18.5 us). More if a row would need more chunks than
+  // the workspace holds.
+  int64_t nvec_max = 0, grid1 = 0;
+  for (int m = 0; m < a.M; ++m) {
+    const int64_t nv = (a.n[m] + VE - 1) / VE;
+    nvec_max = std::max<int64_t>(nvec_max, nv);
+    grid1 += std::max<int64_t>(1, (nv + kBatchVec - 1) / kBatchVec);
+  }
+  grid1 *= a.B;
+  const int64_t resident = 3 * (int64_t)std::max(1, sm_count);
+  const int64_t wanted = (grid1 > resident && grid1 <= 4 * resident) ? 2 : 1;
+  const int64_t batches = std::max<int64_t>(
+      wanted, (nvec_max + (int64_t)kBatchVec * kMaxChunks - 1) / ((int64_t)kBatchVec * kMaxChunks));
   if (batches > INT32_MAX / kBatchVec) return false;
   a.vpc = (int)(batches * kBatchVec);
   int acc = 0;
