@@ -247,16 +247,8 @@ def dmd_residual_scale(zhat0: np.ndarray, x0_teacher_hat: np.ndarray) -> np.ndar
     return np.sum(np.abs(zhat0 - x0_teacher_hat), axis=1) / n
 
 
-def dmd_objective(zhat0, x0_teacher_hat, x0_fake, eps_dmd, weight, lambda_dmd=1.0,
-                  dtype="f64") -> Dict[str, object]:
-    """Joint DMD loss  L = sum_m w_m sum_i (Delta_i^m)^2,
-    Delta = zhat0 - sg(zhat0 - g_bar_DMD), g_bar_DMD = g_DMD / (c_DMD + eps_DMD),
-    g_DMD = x0_fake - x0_T at the re-noised sample  ([zh] 四; [en] Eq. 11-12).
-
-    The reduction over latent elements is a sum, not a mean ([zh] 四).
-    Returns loss [B] (times lambda_dmd), cdmd [B, M] and grad_zhat0 (list).
-    """
-    zh, yT, yF = (_f64_list(a, dtype) for a in (zhat0, x0_teacher_hat, x0_fake))
+def _dmd_core(zh, yT, yF, eps_dmd, weight, lambda_dmd):
+    """The DMD terms on float64 arrays (lists of [B, N_m]); see dmd_objective."""
     B, M = zh[0].shape[0], len(zh)
     loss = np.zeros(B)
     cdmd = np.zeros((B, M))
@@ -272,6 +264,45 @@ def dmd_objective(zhat0, x0_teacher_hat, x0_fake, eps_dmd, weight, lambda_dmd=1.
         # chain rule: dL/dDelta = 2 w Delta; dDelta/dzhat0 = 1 (the sg term is constant)
         grads.append(lambda_dmd * 2.0 * weight[m] * delta)
     return {"loss": lambda_dmd * loss, "cdmd": cdmd, "grad_zhat0": grads}
+
+
+def dmd_objective(zhat0, x0_teacher_hat, x0_fake, eps_dmd, weight, lambda_dmd=1.0,
+                  dtype="f64") -> Dict[str, object]:
+    """Joint DMD loss  L = sum_m w_m sum_i (Delta_i^m)^2,
+    Delta = zhat0 - sg(zhat0 - g_bar_DMD), g_bar_DMD = g_DMD / (c_DMD + eps_DMD),
+    g_DMD = x0_fake - x0_T at the re-noised sample  ([zh] 四; [en] Eq. 11-12).
+
+    The reduction over latent elements is a sum, not a mean ([zh] 四).
+    Returns loss [B] (times lambda_dmd), cdmd [B, M] and grad_zhat0 (list).
+    """
+    zh, yT, yF = (_f64_list(a, dtype) for a in (zhat0, x0_teacher_hat, x0_fake))
+    return _dmd_core(zh, yT, yF, eps_dmd, weight, lambda_dmd)
+
+
+# ----------------------------------------------------------------------------
+# classifier-free guidance of the teacher  ([zh] 四, 七; [en] section 3)
+# ----------------------------------------------------------------------------
+
+def cfg_prediction(cond: np.ndarray, uncond: np.ndarray, scale: float) -> np.ndarray:
+    """The guided teacher prediction uncond + s (cond - uncond).
+
+    The pages state that the teacher's prediction is computed with classifier-free
+    guidance, at scale 3.0 for video and 5.0 for audio, without printing the formula;
+    this is the standard guidance extrapolation from the unconditional prediction
+    through the conditional one (the reading is listed with the design notes).
+    """
+    return uncond + scale * (cond - uncond)
+
+
+def dmd_objective_cfg(zhat0, x0_teacher_hat_cond, x0_teacher_hat_uncond, guidance, x0_fake,
+                      eps_dmd, weight, lambda_dmd=1.0, dtype="f64") -> Dict[str, object]:
+    """The DMD terms with the teacher prediction at the re-noised sample guided per
+    modality: y_T^m = cfg_prediction(cond^m, uncond^m, guidance[m]), in float64 from the
+    stored inputs; then exactly dmd_objective."""
+    zh, yc, yu, yF = (_f64_list(a, dtype) for a in (zhat0, x0_teacher_hat_cond,
+                                                    x0_teacher_hat_uncond, x0_fake))
+    yT = [cfg_prediction(c, u, float(g)) for c, u, g in zip(yc, yu, guidance)]
+    return _dmd_core(zh, yT, yF, eps_dmd, weight, lambda_dmd)
 
 
 # ----------------------------------------------------------------------------
@@ -303,3 +334,48 @@ def stage3_objective(z_t, x0_teacher, x0_student, x0_tangent, t,
             "grad_x0_student": a["grad_x0_student"], "grad_zhat0": grad_dmd,
             "g": a["g"], "valid": ok}
 
+
+
+def stage3_objective_cfg(z_t, x0_teacher, x0_student, x0_tangent, t,
+                         zhat0, x0_teacher_hat_cond, x0_teacher_hat_uncond, guidance, x0_fake,
+                         beta, gamma, eps_scm, eps_dmd, weight,
+                         lambda_scm, lambda_dmd, dtype="f64") -> Dict[str, object]:
+    """stage3_objective with the DMD teacher prediction guided per modality
+    (dmd_objective_cfg)."""
+    a = scm_objective(z_t, x0_teacher, x0_student, x0_tangent, t, beta, gamma, eps_scm,
+                      weight, lambda_scm, dtype)
+    b = dmd_objective_cfg(zhat0, x0_teacher_hat_cond, x0_teacher_hat_uncond, guidance, x0_fake,
+                          eps_dmd, weight, lambda_dmd, dtype)
+    ok = a["valid"]
+    cdmd = b["cdmd"].copy()
+    cdmd[~ok] = np.nan
+    loss_dmd = b["loss"].copy()
+    loss_dmd[~ok] = np.nan
+    grad_dmd = []
+    for g in b["grad_zhat0"]:
+        g = g.copy()
+        g[~ok] = np.nan
+        grad_dmd.append(g)
+    return {"loss": a["loss"] + b["loss"], "loss_scm": a["loss"], "loss_dmd": loss_dmd,
+            "norm": a["norm"], "cdmd": cdmd,
+            "grad_x0_student": a["grad_x0_student"], "grad_zhat0": grad_dmd,
+            "g": a["g"], "valid": ok}
+
+
+# ----------------------------------------------------------------------------
+# TrigFlow -> rectified-flow wrapper  ([zh] 4.2; [en] Eq. 16)
+# ----------------------------------------------------------------------------
+
+def trigflow_to_rf(z_trig: Sequence[np.ndarray], t: np.ndarray):
+    """z_rf = z_trig / (cos t + sin t) per modality and t_rf = sin t / (cos t + sin t) per
+    sample ([zh] 4.2; [en] Eq. 16). Returns (list of z_rf, t_rf [B])."""
+    c, s = _trig(t)
+    return [z / (c + s) for z in z_trig], (s / (c + s)).reshape(-1)
+
+
+def noise_rf(z0, eps, t, dtype: str):
+    """The noising step and the wrapper on stored inputs: z_t and z_rf, each computed in
+    float64 from z0 and eps and rounded once to the storage type, and t_rf in float64."""
+    zt = trigflow_noise(_f64_list(z0, dtype), _f64_list(eps, dtype), t)
+    zrf, trf = trigflow_to_rf(zt, t)
+    return [encode(z, dtype) for z in zt], [encode(z, dtype) for z in zrf], trf

@@ -348,10 +348,95 @@ def pin_domain(orc):
     assert np.all(np.isnan(out["grad_x0_student"][0][0])) and np.all(np.isfinite(out["grad_x0_student"][0][1]))
 
 
+def pin_rf_wrapper(orc):
+    """The rectified-flow reading of a TrigFlow sample: with t_rf = s/(c+s),
+    z_rf = (1 - t_rf) z0 + t_rf eps (a straight line from data to noise);
+    t_rf / (1 - t_rf) = tan t; t = pi/4 halves the sum z0 + eps; t = 0 and pi/2 give
+    z0 and eps; t_rf rises strictly with t."""
+    r = _rng(43)
+    z0 = [r.normal(size=(4, 29)), r.normal(size=(4, 7))]
+    eps = [r.normal(size=(4, 29)), r.normal(size=(4, 7))]
+    t = np.array([0.05, 0.6, 1.1, 1.5])
+    zt = orc.trigflow_noise(z0, eps, t)
+    zrf, trf = orc.trigflow_to_rf(zt, t)
+    for m in range(2):
+        _close(zrf[m], (1 - trf)[:, None] * z0[m] + trf[:, None] * eps[m], rtol=1e-13, atol=1e-15)
+    _close(trf / (1 - trf), np.tan(t), rtol=1e-13)
+    assert np.all(np.diff(trf) > 0)
+    zq, tq = orc.trigflow_to_rf(orc.trigflow_noise(z0, eps, np.full(4, math.pi / 4)), np.full(4, math.pi / 4))
+    _close(tq, np.full(4, 0.5), rtol=1e-15)
+    _close(zq[0], 0.5 * (z0[0] + eps[0]), rtol=1e-13, atol=1e-15)
+    te = np.array([0.0, math.pi / 2, 0.0, math.pi / 2])
+    ze, tre = orc.trigflow_to_rf(orc.trigflow_noise(z0, eps, te), te)
+    _close(tre, np.array([0.0, 1.0, 0.0, 1.0]), rtol=0, atol=1e-15)
+    _close(ze[1][0], z0[1][0], rtol=0, atol=0)
+    _close(ze[1][1], eps[1][1], rtol=0, atol=1e-15)
+    # stored path: both outputs rounded once; at t = pi/4 with eps = 0 the RF sample is
+    # exactly z0 / 2, and the TrigFlow one is z0 / sqrt 2 rounded once
+    zb = orc.round_to_bf16_bits(np.array([[1.0, 0.5, -3.0, 0.375]]))
+    eb = orc.round_to_bf16_bits(np.zeros((1, 4)))
+    zt_b, zrf_b, trf_b = orc.noise_rf([zb], [eb], np.array([math.pi / 4]), "bf16")
+    assert np.array_equal(zrf_b[0], orc.round_to_bf16_bits(np.array([[0.5, 0.25, -1.5, 0.1875]])))
+    assert np.array_equal(zt_b[0], orc.round_to_bf16_bits(np.array([[1.0, 0.5, -3.0, 0.375]]) / math.sqrt(2)))
+    _close(trf_b, np.array([0.5]), rtol=1e-15)
+
+
+def _cfg_inputs(seed, B=3, numels=(40, 12)):
+    r = _rng(seed)
+    zh = [r.normal(size=(B, n)) for n in numels]
+    yc = [x + r.normal(0, 0.1, size=x.shape) for x in zh]
+    yu = [x + r.normal(0, 0.1, size=x.shape) for x in zh]
+    yF = [y + r.normal(0, 0.1, size=y.shape) for y in yc]
+    return zh, yc, yu, yF
+
+
+def pin_cfg_teacher(orc):
+    """Guided teacher: scale 1 gives the conditional prediction and 0 the unconditional
+    one; equal predictions make the scale irrelevant; a closed form with constant
+    offsets (uncond = zhat0 + a, cond = zhat0 + b, fake = zhat0 + f) at the page's video
+    and audio scales 3 and 5: c = |a + s (b - a)|, grad = 2 lam w (f - a - s (b - a)) / (c + eps);
+    the stage-3 sum with guidance is the sCM terms plus the guided DMD terms."""
+    zh, yc, yu, yF = _cfg_inputs(47)
+    w, eps, lam = (1.0, 4.0), 1e-6, 0.25
+    for scale, yT in ((1.0, yc), (0.0, yu)):
+        a = orc.dmd_objective_cfg(zh, yc, yu, (scale, scale), yF, eps, w, lam)
+        b = orc.dmd_objective(zh, yT, yF, eps, w, lam)
+        _close(a["loss"], b["loss"], rtol=1e-14)
+        _close(a["cdmd"], b["cdmd"], rtol=1e-14)
+    a = orc.dmd_objective_cfg(zh, yc, yc, (3.0, 5.0), yF, eps, w, lam)
+    b = orc.dmd_objective(zh, yc, yF, eps, w, lam)
+    _close(a["loss"], b["loss"], rtol=1e-14)
+    B, N = 2, 64
+    r = _rng(53)
+    offs = ((0.1, 0.3, 0.5), (-0.2, 0.05, 0.4))  # (a, b, f) per modality
+    z = [r.normal(size=(B, N)) for _ in range(2)]
+    out = orc.dmd_objective_cfg(z, [z[m] + offs[m][1] for m in range(2)],
+                                [z[m] + offs[m][0] for m in range(2)], (3.0, 5.0),
+                                [z[m] + offs[m][2] for m in range(2)], 1e-3, w, lam)
+    loss = np.zeros(B)
+    for m, (sc, (ao, bo, fo)) in enumerate(zip((3.0, 5.0), offs)):
+        d = ao + sc * (bo - ao)
+        c = abs(d)
+        _close(out["cdmd"][:, m], np.full(B, c), rtol=1e-12)
+        k = (fo - d) / (c + 1e-3)
+        _close(out["grad_zhat0"][m], np.full((B, N), 2 * lam * w[m] * k), rtol=1e-10)
+        loss += lam * w[m] * N * k * k
+    _close(out["loss"], loss, rtol=1e-10)
+    sz, xT, xS, tan, t = _scm_inputs(59)
+    s3 = orc.stage3_objective_cfg(sz, xT, xS, tan, t, zh, yc, yu, (3.0, 5.0), yF,
+                                  1.0, 0.9, 1e-6, 1e-6, w, 1.0, 0.25)
+    a = orc.scm_objective(sz, xT, xS, tan, t, 1.0, 0.9, 1e-6, w, 1.0)
+    b = orc.dmd_objective_cfg(zh, yc, yu, (3.0, 5.0), yF, 1e-6, w, 0.25)
+    _close(s3["loss"], a["loss"] + b["loss"], rtol=1e-14)
+    for m in range(2):
+        _close(s3["grad_zhat0"][m], b["grad_zhat0"][m], rtol=0)
+
+
 PINS = [pin_jvp_finite_difference, pin_jvp_autodiff, pin_direction_symbolic,
         pin_direction_closed_forms, pin_norm_and_loss, pin_zero_direction,
         pin_scm_gradient_autograd, pin_dmd_closed_form, pin_dmd_autograd,
-        pin_stage3_composition, pin_bf16_rounding, pin_noise, pin_domain]
+        pin_stage3_composition, pin_bf16_rounding, pin_noise, pin_domain, pin_rf_wrapper,
+        pin_cfg_teacher]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -461,6 +546,34 @@ def _mut_dmd_mean_loss(m):
     m.dmd_objective = dmd
 
 
+def _mut_rf_norm_divisor(m):
+    # divide by the rotation's norm sqrt(c^2 + s^2) = 1 instead of c + s
+    m.trigflow_to_rf = lambda z, t: ([x.copy() for x in z],
+                                     (np.sin(np.asarray(t, np.float64)) / 1.0).reshape(-1))
+
+
+def _mut_rf_time_cos(m):
+    orig = m.trigflow_to_rf
+
+    def rf(z, t):
+        zr, _ = orig(z, t)
+        c, s = m._trig(t)
+        return zr, (c / (c + s)).reshape(-1)
+    m.trigflow_to_rf = rf
+
+
+def _mut_cfg_swapped(m):
+    m.cfg_prediction = lambda cond, uncond, scale: cond + scale * (uncond - cond)
+
+
+def _mut_cfg_scale_order(m):
+    orig = m.dmd_objective_cfg
+
+    def cfg(zh, yc, yu, g, yF, *a, **k):
+        return orig(zh, yc, yu, tuple(reversed(tuple(g))), yF, *a, **k)
+    m.dmd_objective_cfg = cfg
+
+
 MUTANTS = {
     "jvp_tangent_sign": _mut_jvp_tangent_sign,
     "jvp_no_ct": _mut_jvp_no_ct,
@@ -477,6 +590,10 @@ MUTANTS = {
     "noise_swap_cos_sin": _mut_noise_swap,
     "bf16_double_rounding": _mut_bf16_double_rounding,
     "scm_grad_no_inv_sin": _mut_scm_grad_no_inv_sin,
+    "rf_norm_divisor": _mut_rf_norm_divisor,
+    "rf_time_cos": _mut_rf_time_cos,
+    "cfg_swapped": _mut_cfg_swapped,
+    "cfg_scale_order": _mut_cfg_scale_order,
 }
 
 
