@@ -4,7 +4,10 @@ One step = one pass of the whole hot path over one batch of synthetic inputs:
 TrigFlow noising of (z0, eps) and of (zhat0, eps'), then the fused stage-3
 sCM + DMD objective (forward + gradient), all through the C ABI. The default
 workload is the 512x768 stage-3 shape (B=4, video [128,16,16,24], audio
-[126,128], bf16 inputs, float32 gradients).
+[126,128], bf16 inputs, float32 gradients). The workload stage3_cfg_rf_512x768_bf16
+extends the step with the rectified-flow wrapper in the noising (z_rf and t_rf
+written beside z_t) and a guided DMD teacher (conditional and unconditional
+predictions read in place of one).
 
 Prints one JSON line. `value` is the whole-job throughput in GB/s of algorithmic
 HBM bytes (each input read once, each output written once) with inputs resident
@@ -58,23 +61,39 @@ def elem_size(dtype: str) -> int:
 def bytes_per_element(call: str, dtype: str) -> int:
     """Each input read once, each output written once; gradients are float32."""
     e = elem_size(dtype)
-    return {"noise": 3 * e, "scm": 4 * e + 4, "dmd": 3 * e + 4, "stage3": 7 * e + 2 * 4}[call]
+    return {"noise": 3 * e, "noise_rf": 4 * e, "scm": 4 * e + 4, "dmd": 3 * e + 4,
+            "stage3": 7 * e + 2 * 4, "stage3_cfg": 8 * e + 2 * 4}[call]
+
+
+def is_stage3(wl: S.Workload) -> bool:
+    return wl.mode in (S.STAGE3, S.STAGE3_CFG)
 
 
 def step_bytes(wl: S.Workload) -> dict:
     n = wl.batch * sum(wl.numels)
     out = {"elements": n}
-    if wl.mode == S.STAGE3:
-        out["noise"] = 2 * n * bytes_per_element("noise", wl.dtype)
-        out["objective"] = n * bytes_per_element("stage3", wl.dtype)
+    nz = bytes_per_element("noise_rf" if wl.rf_wrapper else "noise", wl.dtype)
+    if is_stage3(wl):
+        out["noise"] = 2 * n * nz + (2 * 4 * wl.batch if wl.rf_wrapper else 0)
+        out["objective"] = n * bytes_per_element(wl.mode, wl.dtype)
     elif wl.mode == S.SCM:
-        out["noise"] = n * bytes_per_element("noise", wl.dtype)
+        out["noise"] = n * nz + (4 * wl.batch if wl.rf_wrapper else 0)
         out["objective"] = n * bytes_per_element("scm", wl.dtype)
     else:
         out["noise"] = 0
         out["objective"] = n * bytes_per_element("dmd", wl.dtype)
     out["step"] = out["noise"] + out["objective"]
     return out
+
+
+def input_fields(wl: S.Workload) -> list:
+    """The host inputs of one step, per modality (the timesteps apart)."""
+    f = ["z0", "eps", "x0_teacher", "x0_student", "x0_tangent"]
+    if is_stage3(wl):
+        f += ["zhat0", "eps_hat", "x0_teacher_hat", "x0_fake"]
+    if wl.mode == S.STAGE3_CFG:
+        f += ["x0_teacher_hat_uncond"]
+    return f
 
 
 def measured_peak():
@@ -265,9 +284,7 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     # rotating input sets: together at least 3x the L2 size, so no step finds its inputs in L2
     set_bytes = nb["step"] + 2 * wl.batch * sum(wl.numels) * elem_size(dt)
     R = max(2, math.ceil(3 * l2 / set_bytes))
-    fields_in = ["z0", "eps", "x0_teacher", "x0_student", "x0_tangent"]
-    if wl.mode == S.STAGE3:
-        fields_in += ["zhat0", "eps_hat", "x0_teacher_hat", "x0_fake"]
+    fields_in = input_fields(wl)
 
     def to_dev(a):
         if dt == "bf16":
@@ -284,9 +301,14 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
         d["t"] = torch.from_numpy(inp.t).to(dev)
         d["zt"] = [torch.empty_like(x) for x in d["z0"]]
         d["gS"] = [torch.empty(x.shape, dtype=torch.float32, device=dev) for x in d["z0"]]
-        if wl.mode == S.STAGE3:
+        if is_stage3(wl):
             d["zht"] = [torch.empty_like(x) for x in d["zhat0"]]
             d["gD"] = [torch.empty(x.shape, dtype=torch.float32, device=dev) for x in d["z0"]]
+        if wl.rf_wrapper:
+            d["zrf"] = [torch.empty_like(x) for x in d["z0"]]
+            d["t_rf"] = torch.empty(wl.batch, device=dev)
+            if is_stage3(wl):
+                d["zhrf"] = [torch.empty_like(x) for x in d["zhat0"]]
         d["loss"] = torch.empty(wl.batch, device=dev)
         d["norm"] = torch.empty(wl.batch * M, device=dev)
         d["cdmd"] = torch.empty(wl.batch * M, device=dev)
@@ -296,7 +318,15 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     torch.cuda.synchronize()
 
     def objective(d, stream=None):
-        if wl.mode == S.STAGE3:
+        if wl.mode == S.STAGE3_CFG:
+            t2va.stage3_objective_cfg(
+                d["zt"], d["x0_teacher"], d["x0_student"], d["x0_tangent"], d["t"], d["zhat0"],
+                d["x0_teacher_hat"], d["x0_teacher_hat_uncond"], d["x0_fake"], guidance=wl.guidance,
+                beta=wl.beta, gamma=wl.gamma, eps_scm=wl.eps_scm, eps_dmd=wl.eps_dmd,
+                weight=wl.weight, lambda_scm=wl.lambda_scm, lambda_dmd=wl.lambda_dmd,
+                grad_x0_student=d["gS"], grad_zhat0=d["gD"], loss=d["loss"], norm=d["norm"],
+                cdmd=d["cdmd"], workspace=ws, status=status, stream=stream)
+        elif wl.mode == S.STAGE3:
             t2va.stage3_objective(d["zt"], d["x0_teacher"], d["x0_student"], d["x0_tangent"], d["t"],
                                   d["zhat0"], d["x0_teacher_hat"], d["x0_fake"], beta=wl.beta,
                                   gamma=wl.gamma, eps_scm=wl.eps_scm, eps_dmd=wl.eps_dmd,
@@ -313,11 +343,14 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     def noise(d, stream=None):
         # both noisings (z0 -> z_t and the on-policy zhat0 -> zhat_t) share the per-sample t,
         # so they go to the library as one call over four latents
-        if wl.mode == S.STAGE3:
-            t2va.noise(d["z0"] + d["zhat0"], d["eps"] + d["eps_hat"], d["zt"] + d["zht"], d["t"],
-                       status=status, stream=stream)
+        z0, eps, zt = d["z0"], d["eps"], d["zt"]
+        if is_stage3(wl):
+            z0, eps, zt = z0 + d["zhat0"], eps + d["eps_hat"], zt + d["zht"]
+        if wl.rf_wrapper:
+            zrf = d["zrf"] + (d["zhrf"] if is_stage3(wl) else [])
+            t2va.noise_rf(z0, eps, zt, zrf, d["t"], t_rf=d["t_rf"], status=status, stream=stream)
         else:
-            t2va.noise(d["z0"], d["eps"], d["zt"], d["t"], status=status, stream=stream)
+            t2va.noise(z0, eps, zt, d["t"], status=status, stream=stream)
 
     launches_per_step = 3   # t2va_noise + the objective's two kernels
 
@@ -328,7 +361,7 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     cap_stream = torch.cuda.Stream(device=dev)
     cap_stream.wait_stream(torch.cuda.current_stream())
 
-    def capture(nsteps, offset=0, objective_only=False):
+    def capture(nsteps, offset=0, objective_only=False, noise_only=False):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(cap_stream):
             with torch.cuda.graph(g, stream=cap_stream):
@@ -336,7 +369,8 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
                     d = sets[(offset + i) % R]
                     if not objective_only:
                         noise(d, cap_stream)
-                    objective(d, cap_stream)
+                    if not noise_only:
+                        objective(d, cap_stream)
         return g
 
     # eager warm-up of every set once (also first-call attribute setup), then capture
@@ -351,6 +385,7 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     g_warm = capture(W) if W > 0 else None
     # the dominant kernel alone: back-to-back objective launches over the same rotating sets
     g_obj = capture(S_steps, objective_only=True)
+    g_noise = capture(S_steps, noise_only=True)
     torch.cuda.synchronize()
 
     # clock ramp (the GPU leaves its idle clocks only under sustained load), then W warm-up steps
@@ -404,6 +439,15 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
         o_end.record(cap_stream)
     cap_stream.synchronize()
     obj_mean_ms = o_start.elapsed_time(o_end) / (obj_reps * S_steps)
+    # the same for the noising kernel
+    with torch.cuda.stream(cap_stream):
+        g_noise.replay()
+        o_start.record(cap_stream)
+        for _ in range(obj_reps):
+            g_noise.replay()
+        o_end.record(cap_stream)
+    cap_stream.synchronize()
+    noise_mean_ms = o_start.elapsed_time(o_end) / (obj_reps * S_steps)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during the benchmark")
 
@@ -415,7 +459,7 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     clocks = sampler.summary(h0, h1)
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(args, wl, host0, sets[0], ws, status, noise, objective, dev, nb, world, dist)
+    e2e = run_e2e(args, wl, host0, sets[:2], status, noise, objective, dev, nb, world, dist)
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -423,6 +467,8 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
         "vs_baseline": None, "dtype": dt, "data": "synthetic",
         "config": {"workload": wl.name, "global_batch": wl.batch * world, "per_gpu_batch": wl.batch,
                    "latent_shapes": [list(s) for s in wl.shapes], "mode": wl.mode,
+                   "rf_wrapper": wl.rf_wrapper,
+                   **({"guidance": list(wl.guidance)} if wl.mode == S.STAGE3_CFG else {}),
                    "elements_per_step": nb["elements"] * world,
                    "algorithmic_bytes_per_step": nb["step"] * world,
                    "parallelism": f"replicas x{world} (samples sharded by rank, no collective)",
@@ -433,7 +479,9 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
                    "clock_ramp_s": args.clock_ramp_seconds},
         "elements_per_s": nb["elements"] * world * K / (elapsed_ms * 1e-3),
         "hbm_fraction_of_step": round(value / world / peak, 4),
-        "roofline": {"kernel": ("t2va stage-3 objective" if wl.mode == S.STAGE3 else "t2va sCM objective")
+        "roofline": {"kernel": {S.STAGE3: "t2va stage-3 objective",
+                                S.STAGE3_CFG: "t2va guided stage-3 objective",
+                                S.SCM: "t2va sCM objective"}.get(wl.mode, "t2va objective")
                                + " call (k_sums + k_grads)",
                      "bound": "hbm", "achieved": round(obj_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(obj_gbs / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
@@ -446,6 +494,13 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
                                       "around the region on the launching stream; includes the "
                                       "launch-to-launch gap",
                      "frac_of_nominal_8TBps": round(obj_gbs / 8000.0, 4)},
+        "noise_kernel": {"kernel": "t2va_noise_rf (k_noise, z_t and z_rf)" if wl.rf_wrapper
+                                   else "t2va_noise (k_noise)",
+                         "achieved": round(nb["noise"] / (noise_mean_ms * 1e-3) / 1e9, 2),
+                         "unit": "GB/s", "frac": round(nb["noise"] / (noise_mean_ms * 1e-3) / 1e9 / peak, 4),
+                         "algorithmic_bytes_per_launch": nb["noise"],
+                         "mean_launch_us": round(noise_mean_ms * 1e3, 3),
+                         "launch_timing": "as for the roofline kernel"},
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
@@ -453,14 +508,16 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     return result
 
 
-def run_e2e(args, wl, host0, d0, ws, status, noise, objective, dev, nb, world, dist):
-    """Same step with pinned host inputs copied in and gradients/losses copied out."""
+def run_e2e(args, wl, host0, dsets, status, noise, objective, dev, nb, world, dist):
+    """The same steps with host buffers: every step copies its inputs in from pinned host
+    memory and its gradients and losses back out. Steps are pipelined the way a data
+    loader feeds a training loop: two device buffer sets alternate, and the copies in,
+    the compute and the copies out run on three streams ordered by events, so step i+1's
+    inputs arrive while step i computes and step i-1's results drain."""
     import torch
 
-    steps = max(3, min(args.steps, args.e2e_steps))
-    fields = ["z0", "eps", "x0_teacher", "x0_student", "x0_tangent", "t"]
-    if wl.mode == S.STAGE3:
-        fields += ["zhat0", "eps_hat", "x0_teacher_hat", "x0_fake"]
+    steps = max(4, min(args.steps, args.e2e_steps))
+    fields = input_fields(wl) + ["t"]
     pinned = {}
     h2d = 0
     for f in fields:
@@ -474,41 +531,62 @@ def run_e2e(args, wl, host0, d0, ws, status, noise, objective, dev, nb, world, d
                 ts = [torch.from_numpy(a).pin_memory() for a in arrs]
         pinned[f] = ts
         h2d += sum(x.numel() * x.element_size() for x in ts)
-    outs = ["gS", "loss"] + (["gD"] if wl.mode == S.STAGE3 else [])
-    host_out = {k: [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (d0[k] if isinstance(d0[k], list) else [d0[k]])]
-                for k in outs}
-    d2h = sum(x.numel() * x.element_size() for v in host_out.values() for x in v)
-    stream = torch.cuda.Stream(device=dev)
+    outs = ["gS", "loss"] + (["gD"] if is_stage3(wl) else [])
 
-    def one():
-        with torch.cuda.stream(stream):
+    def as_list(v):
+        return v if isinstance(v, list) else [v]
+
+    host_out = [{k: [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in as_list(d[k])]
+                 for k in outs} for d in dsets]
+    d2h = sum(x.numel() * x.element_size() for v in host_out[0].values() for x in v)
+    s_in, s_cmp, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in dsets]
+    ev_cmp = [torch.cuda.Event() for _ in dsets]
+    ev_out = [torch.cuda.Event() for _ in dsets]
+
+    def step(i):
+        k = i % len(dsets)
+        d = dsets[k]
+        with torch.cuda.stream(s_in):
+            if i >= len(dsets):
+                s_in.wait_event(ev_cmp[k])    # the compute that last read these inputs is done
             for f in fields:
-                dst = [d0["t"]] if f == "t" else d0[f]
+                dst = [d["t"]] if f == "t" else d[f]
                 for a, b in zip(dst, pinned[f]):
                     a.copy_(b, non_blocking=True)
-            noise(d0, stream)
-            objective(d0, stream)
-            for k in outs:
-                src = d0[k] if isinstance(d0[k], list) else [d0[k]]
-                for a, b in zip(host_out[k], src):
+            ev_in[k].record(s_in)
+        with torch.cuda.stream(s_cmp):
+            s_cmp.wait_event(ev_in[k])
+            if i >= len(dsets):
+                s_cmp.wait_event(ev_out[k])   # the copy-out that last read these outputs is done
+            noise(d, s_cmp)
+            objective(d, s_cmp)
+            ev_cmp[k].record(s_cmp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_cmp[k])
+            for key in outs:
+                for a, b in zip(host_out[k][key], as_list(d[key])):
                     a.copy_(b, non_blocking=True)
+            ev_out[k].record(s_out)
 
-    one()
-    stream.synchronize()
+    for i in range(len(dsets)):
+        step(i)
+    torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        one()
-    e1.record(stream)
-    stream.synchronize()
+    e0.record(s_in)
+    for i in range(steps):
+        step(i)
+    e1.record(s_out)
+    torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     assert int(status.item()) == 0
     return {"value": round(whole_job_gbs(world, nb["step"], steps, ms), 3), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": ms / steps}
+            "ms_per_step": ms / steps,
+            "pipeline": "2 device buffer sets; copy-in, compute and copy-out streams"}
 
 
 # ---------------------------------------------------------------------------
@@ -518,9 +596,20 @@ def run_e2e(args, wl, host0, d0, ws, status, noise, objective, dev, nb, world, d
 def oracle_pass(wl: S.Workload, inp: S.Inputs):
     import oracle
     dt = wl.dtype
-    zt = oracle.noise(inp.z0, inp.eps, inp.t, dt)
-    if wl.mode == S.STAGE3:
-        oracle.noise(inp.zhat0, inp.eps_hat, inp.t, dt)
+    if wl.rf_wrapper:
+        zt = oracle.noise_rf(inp.z0, inp.eps, inp.t, dt)[0]
+        if is_stage3(wl):
+            oracle.noise_rf(inp.zhat0, inp.eps_hat, inp.t, dt)
+    else:
+        zt = oracle.noise(inp.z0, inp.eps, inp.t, dt)
+        if is_stage3(wl):
+            oracle.noise(inp.zhat0, inp.eps_hat, inp.t, dt)
+    if wl.mode == S.STAGE3_CFG:
+        oracle.stage3_objective_cfg(zt, inp.x0_teacher, inp.x0_student, inp.x0_tangent, inp.t,
+                                    inp.zhat0, inp.x0_teacher_hat, inp.x0_teacher_hat_uncond,
+                                    wl.guidance, inp.x0_fake, wl.beta, wl.gamma, wl.eps_scm,
+                                    wl.eps_dmd, wl.weight, wl.lambda_scm, wl.lambda_dmd, dt)
+    elif wl.mode == S.STAGE3:
         oracle.stage3_objective(zt, inp.x0_teacher, inp.x0_student, inp.x0_tangent, inp.t,
                                 inp.zhat0, inp.x0_teacher_hat, inp.x0_fake, wl.beta, wl.gamma,
                                 wl.eps_scm, wl.eps_dmd, wl.weight, wl.lambda_scm, wl.lambda_dmd, dt)

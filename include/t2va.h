@@ -119,6 +119,25 @@ int t2va_noise(int batch, int num_modalities, const t2va_segment* seg, t2va_dtyp
                const void* const* z0, const void* const* eps, void* const* zt,
                const float* t, int* status, cudaStream_t stream);
 
+/* TrigFlow noising fused with the TrigFlow -> rectified-flow wrapper
+ * ([zh] 4.2; [en] Eq. 16), for a backbone trained in the rectified-flow
+ * parameterisation:
+ *   z_t^m  = cos(t_b) z0^m + sin(t_b) eps^m                  (as t2va_noise),
+ *   z_rf^m = z_t^m / (cos t_b + sin t_b),
+ *   t_rf[b] = sin t_b / (cos t_b + sin t_b),
+ * so z_rf = (1 - t_rf) z0 + t_rf eps. Both latents come from one read of z0 and
+ * eps, each rounded once from float32 arithmetic to the latent dtype.
+ * `zt` may be NULL (only z_rf is written); `z_rf` is required; a zt[m] that is the
+ * same buffer as z_rf[m] is an error; either may be the same buffer as z0 or eps
+ * (in place). `t_rf` (device float [batch]) may be NULL. Every finite t is
+ * accepted (t in [0, pi/2] keeps cos t + sin t >= 1); `status` may be NULL; a
+ * non-finite t sets T2VA_STATUS_BAD_TIMESTEP. Reads 2 and writes 1 or 2 elements
+ * per latent element. */
+int t2va_noise_rf(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+                  const void* const* z0, const void* const* eps, void* const* zt,
+                  void* const* z_rf, const float* t, float* t_rf, int* status,
+                  cudaStream_t stream);
+
 /* Joint sCM objective  ([zh] 3.1; [en] Eq. 6). Per sample b and modality m,
  * with c = cos t_b, s = sin t_b and elementwise
  *   F_T = (c z_t - x0_teacher)/s,  F_theta = (c z_t - x0_student)/s,
@@ -190,6 +209,26 @@ int t2va_stage3_objective(int batch, int num_modalities, const t2va_segment* seg
                           float* loss, float* loss_scm, float* loss_dmd, float* norm, float* cdmd,
                           void* workspace, size_t workspace_bytes, int* status,
                           cudaStream_t stream);
+
+/* Stage-3 objective with a guided teacher ([zh] 四 and 七; [en] section 3: the
+ * teacher prediction of the DMD term is computed with classifier-free guidance,
+ * at a scale per modality, 3.0 for video and 5.0 for audio in the paper's
+ * training). Per element, in float32,
+ *   y_T = u + guidance[m] (k - u),   k = x0_teacher_hat_cond, u = x0_teacher_hat_uncond,
+ * and then exactly t2va_stage3_objective with x0_teacher_hat = y_T. `guidance`
+ * is a host array of num_modalities finite floats; x0_teacher_hat_uncond has
+ * the geometry of the other latents. The guided prediction is never stored:
+ * each pass reads k and u (eight inputs for the sums, seven for the gradients). */
+int t2va_stage3_objective_cfg(
+    int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+    const void* const* z_t, const void* const* x0_teacher, const void* const* x0_student,
+    const void* const* x0_student_tangent, const float* t, const void* const* zhat0,
+    const void* const* x0_teacher_hat_cond, const void* const* x0_teacher_hat_uncond,
+    const float* guidance, const void* const* x0_fake, float beta, float gamma, float eps_scm,
+    float eps_dmd, const float* weight, float lambda_scm, float lambda_dmd,
+    float* const* grad_x0_student, float* const* grad_zhat0, int accumulate, float* loss,
+    float* loss_scm, float* loss_dmd, float* norm, float* cdmd, void* workspace,
+    size_t workspace_bytes, int* status, cudaStream_t stream);
 
 /* Bytes of the library's own scratch array used by
  * t2va_stage3_objective_noalloc (1 MiB). Every GPU that loads the library holds

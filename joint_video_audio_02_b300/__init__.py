@@ -12,8 +12,10 @@ from .binding import (  # noqa: F401
     load,
     new_workspace,
     noise,
+    noise_rf,
     scm_objective,
     stage3_objective,
+    stage3_objective_cfg,
     stage3_objective_noalloc,
     workspace_bytes,
     workspace_init,

@@ -35,7 +35,7 @@ NOALLOC_SCRATCH_BYTES = 1 << 20   # T2VA_NOALLOC_SCRATCH_BYTES
 
 EXPORTED = ("t2va_error_string", "t2va_abi_version", "t2va_workspace_bytes", "t2va_workspace_init",
             "t2va_noise", "t2va_scm_objective", "t2va_dmd_objective", "t2va_stage3_objective",
-            "t2va_stage3_objective_noalloc")
+            "t2va_stage3_objective_noalloc", "t2va_noise_rf", "t2va_stage3_objective_cfg")
 
 
 class Segment(ctypes.Structure):
@@ -79,6 +79,12 @@ def _declare(lib):
                                                   c_float, c_float, c_float, c_float, P, c_float,
                                                   c_float, P, P, c_int, P, P, P, P, P, P, P]
     lib.t2va_stage3_objective_noalloc.restype = c_int
+    lib.t2va_noise_rf.argtypes = [c_int, c_int, seg, c_int, P, P, P, P, P, P, P, P]
+    lib.t2va_noise_rf.restype = c_int
+    lib.t2va_stage3_objective_cfg.argtypes = [c_int, c_int, seg, c_int, P, P, P, P, P, P, P, P, P, P,
+                                              c_float, c_float, c_float, c_float, P, c_float, c_float,
+                                              P, P, c_int, P, P, P, P, P, P, c_size_t, P, P]
+    lib.t2va_stage3_objective_cfg.restype = c_int
 
 
 def load(path: Optional[str] = None):
@@ -189,6 +195,25 @@ def noise(z0: Sequence[torch.Tensor], eps: Sequence[torch.Tensor], zt: Sequence[
                              _opt(status), _stream(stream)), "t2va_noise")
 
 
+def noise_rf(z0: Sequence[torch.Tensor], eps: Sequence[torch.Tensor],
+             zt: Optional[Sequence[torch.Tensor]], z_rf: Sequence[torch.Tensor], t: torch.Tensor,
+             t_rf: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+             stream=None):
+    """TrigFlow noising and its rectified-flow form in one pass (t2va_noise_rf): z_t
+    into `zt` (may be None), z_t / (cos t + sin t) into `z_rf`, and
+    sin t / (cos t + sin t) into `t_rf` (may be None)."""
+    B, M = int(t.shape[0]), len(z0)
+    groups = [z0, eps, z_rf] + ([zt] if zt is not None else [])
+    segs = _segments(groups, B)
+    dt = _dtype_code(z0[0].dtype)
+    _f32(t, "t")
+    if t_rf is not None:
+        _f32(t_rf, "t_rf")
+    _check(load().t2va_noise_rf(B, M, segs, dt, _ptrs(z0), _ptrs(eps),
+                                _ptrs(zt) if zt is not None else None, _ptrs(z_rf), t.data_ptr(),
+                                _opt(t_rf), _opt(status), _stream(stream)), "t2va_noise_rf")
+
+
 def scm_objective(z_t, x0_teacher, x0_student, x0_student_tangent, t, *, beta, gamma, eps_scm,
                   weight, lambda_scm, grad_x0_student, loss, norm=None, accumulate=False,
                   workspace, status, stream=None):
@@ -240,6 +265,32 @@ def stage3_objective(z_t, x0_teacher, x0_student, x0_student_tangent, t, zhat0, 
         loss.data_ptr(), _opt(loss_scm), _opt(loss_dmd), _opt(norm), _opt(cdmd),
         workspace.data_ptr(), workspace.numel() * workspace.element_size(), status.data_ptr(),
         _stream(stream)), "t2va_stage3_objective")
+
+
+def stage3_objective_cfg(z_t, x0_teacher, x0_student, x0_student_tangent, t, zhat0,
+                         x0_teacher_hat_cond, x0_teacher_hat_uncond, x0_fake, *, guidance, beta,
+                         gamma, eps_scm, eps_dmd, weight, lambda_scm, lambda_dmd, grad_x0_student,
+                         grad_zhat0, loss, loss_scm=None, loss_dmd=None, norm=None, cdmd=None,
+                         accumulate=False, workspace, status, stream=None):
+    """stage3_objective with the DMD teacher prediction guided per modality:
+    u + guidance[m] (k - u) from the conditional (k) and unconditional (u) predictions
+    (t2va_stage3_objective_cfg)."""
+    B, M = int(t.shape[0]), len(z_t)
+    segs = _segments([z_t, x0_teacher, x0_student, x0_student_tangent, zhat0, x0_teacher_hat_cond,
+                      x0_teacher_hat_uncond, x0_fake, grad_x0_student, grad_zhat0], B)
+    dt = _dtype_code(z_t[0].dtype)
+    for g in list(grad_x0_student) + list(grad_zhat0):
+        _f32(g, "gradient")
+    w = (c_float * M)(*[float(x) for x in weight])
+    gs = (c_float * M)(*[float(x) for x in guidance])
+    _check(load().t2va_stage3_objective_cfg(
+        B, M, segs, dt, _ptrs(z_t), _ptrs(x0_teacher), _ptrs(x0_student), _ptrs(x0_student_tangent),
+        t.data_ptr(), _ptrs(zhat0), _ptrs(x0_teacher_hat_cond), _ptrs(x0_teacher_hat_uncond), gs,
+        _ptrs(x0_fake), float(beta), float(gamma), float(eps_scm), float(eps_dmd), w,
+        float(lambda_scm), float(lambda_dmd), _ptrs(grad_x0_student), _ptrs(grad_zhat0),
+        int(bool(accumulate)), loss.data_ptr(), _opt(loss_scm), _opt(loss_dmd), _opt(norm),
+        _opt(cdmd), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        status.data_ptr(), _stream(stream)), "t2va_stage3_objective_cfg")
 
 
 def stage3_objective_noalloc(z_t, x0_teacher, x0_student, x0_student_tangent, t, zhat0,

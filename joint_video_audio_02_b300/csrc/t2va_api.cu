@@ -135,6 +135,127 @@ void fill_geometry(ObjectiveArgs& a, int B, int M, const t2va_segment* seg) {
   }
 }
 
+// Plan and launch one noising kernel writing `outputs` (NoiseOut bits). Pointers
+// are checked by the caller.
+int run_noise(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+              const void* const* z0, const void* const* eps, void* const* zt,
+              void* const* zrf, const float* t, float* t_rf, int* status, int outputs,
+              cudaStream_t stream) {
+  NoiseArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.B = batch;
+  a.M = num_modalities;
+  a.t = t;
+  a.t_rf = t_rf;
+  a.status = status;
+  const int VE = dtype == T2VA_BFLOAT16 ? 8 : 4;
+  const int64_t per_cta = noise_vectors_per_cta();
+  int64_t total = 0;
+  for (int m = 0; m < num_modalities; ++m) {
+    a.n[m] = seg[m].numel;
+    a.stride[m] = seg[m].sample_stride;
+    a.z0[m] = z0[m];
+    a.eps[m] = eps[m];
+    a.zt[m] = zt != nullptr ? zt[m] : nullptr;
+    a.zrf[m] = zrf != nullptr ? zrf[m] : nullptr;
+    // CTAs per (sample, modality); an empty modality gets no CTA at all
+    const int64_t vec_ub = (seg[m].numel + VE - 1) / VE;
+    const int64_t chunks = (vec_ub + per_cta - 1) / per_cta;
+    if (chunks > INT32_MAX) return T2VA_ERROR_INVALID_ARGUMENT;
+    a.chunks[m] = chunks > 0 ? (int)chunks : 1;
+    a.block_off[m] = (int)total;
+    total += (int64_t)batch * chunks;
+    if (total > INT32_MAX) return T2VA_ERROR_INVALID_ARGUMENT;
+  }
+  for (int m = num_modalities; m <= kMaxM; ++m) {
+    if (m < kMaxM) a.chunks[m] = 1;
+    a.block_off[m] = (int)total;
+  }
+  // CTA b also writes t_rf[b], so a launch with t_rf has at least B CTAs
+  const int64_t grid = (t_rf != nullptr && total < batch) ? batch : total;
+  if (grid == 0) return T2VA_SUCCESS;
+  if (launch_noise(a, dtype, outputs, (int)grid, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return T2VA_ERROR_CUDA;
+  }
+  return T2VA_SUCCESS;
+}
+
+// The stage-3 entry points: without guidance (x0_teacher_hat_uncond and guidance
+// null), x0_teacher_hat is the teacher prediction; with it, the conditional one.
+int stage3_impl(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+                const void* const* z_t, const void* const* x0_teacher,
+                const void* const* x0_student, const void* const* x0_student_tangent,
+                const float* t,
+                const void* const* zhat0, const void* const* x0_teacher_hat,
+                const void* const* x0_teacher_hat_uncond, const float* guidance,
+                const void* const* x0_fake,
+                float beta, float gamma, float eps_scm, float eps_dmd,
+                const float* weight, float lambda_scm, float lambda_dmd,
+                float* const* grad_x0_student, float* const* grad_zhat0, int accumulate,
+                float* loss, float* loss_scm, float* loss_dmd, float* norm, float* cdmd,
+                void* workspace, size_t workspace_bytes, int* status, cudaStream_t stream) {
+  const int M = num_modalities;
+  T2VA_TRY(check_geometry(batch, M, seg));
+  T2VA_TRY(check_dtype(dtype));
+  if (batch == 0) return T2VA_SUCCESS;
+  for (const void* const* p : {z_t, x0_teacher, x0_student, x0_student_tangent, zhat0,
+                               x0_teacher_hat, x0_fake})
+    T2VA_TRY(check_ptrs(M, seg, p));
+  const bool cfg = x0_teacher_hat_uncond != nullptr;
+  if (cfg) {
+    T2VA_TRY(check_ptrs(M, seg, x0_teacher_hat_uncond));
+    if (guidance == nullptr) return T2VA_ERROR_INVALID_ARGUMENT;
+    for (int m = 0; m < M; ++m)
+      if (!finite(guidance[m])) return T2VA_ERROR_INVALID_ARGUMENT;
+  }
+  T2VA_TRY(check_ptrs(M, seg, reinterpret_cast<const void* const*>(grad_x0_student)));
+  T2VA_TRY(check_ptrs(M, seg, reinterpret_cast<const void* const*>(grad_zhat0)));
+  T2VA_TRY(check_scalar_out(t, true));
+  T2VA_TRY(check_scalar_out(loss, true));
+  for (const float* p : {loss_scm, loss_dmd, norm, cdmd}) T2VA_TRY(check_scalar_out(p, false));
+  T2VA_TRY(check_scalar_out(status, true));
+  T2VA_TRY(check_weights(M, weight));
+  if (!finite(beta) || !(gamma >= 0.f && gamma <= 1.f) || !finite(eps_scm) || !(eps_scm > 0.f) ||
+      !finite(lambda_scm) || !finite(eps_dmd) || !(eps_dmd > 0.f) || !finite(lambda_dmd))
+    return T2VA_ERROR_INVALID_ARGUMENT;
+  ObjectiveArgs a;
+  fill_geometry(a, batch, M, seg);
+  for (int m = 0; m < M; ++m) {
+    a.in[kZt][m] = z_t[m];
+    a.in[kXT][m] = x0_teacher[m];
+    a.in[kXS][m] = x0_student[m];
+    a.in[kXdot][m] = x0_student_tangent[m];
+    a.in[kZh][m] = zhat0[m];
+    a.in[kYT][m] = x0_teacher_hat[m];
+    a.in[kYF][m] = x0_fake[m];
+    if (cfg) {
+      a.in[kYU][m] = x0_teacher_hat_uncond[m];
+      a.cfg[m] = guidance[m];
+    }
+    a.grad_s[m] = grad_x0_student[m];
+    a.grad_d[m] = grad_zhat0[m];
+    if (grad_x0_student[m] == grad_zhat0[m]) a.alias_mask |= 1u << m;
+    a.w[m] = weight[m];
+  }
+  a.t = t;
+  a.beta = beta;
+  a.gamma = gamma;
+  a.eps_s = eps_scm;
+  a.lam_s = lambda_scm;
+  a.eps_d = eps_dmd;
+  a.lam_d = lambda_dmd;
+  a.accumulate = accumulate ? 1 : 0;
+  a.loss = loss;
+  a.loss_s = loss_scm;
+  a.loss_d = loss_dmd;
+  a.norm = norm;
+  a.cdmd = cdmd;
+  a.status = status;
+  return run_objective(a, dtype, cfg ? (kModeStage3 | kModeCfg) : kModeStage3, workspace,
+                      workspace_bytes, stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -185,40 +306,29 @@ int t2va_noise(int batch, int num_modalities, const t2va_segment* seg, t2va_dtyp
   T2VA_TRY(check_ptrs(num_modalities, seg, reinterpret_cast<const void* const*>(zt)));
   T2VA_TRY(check_scalar_out(t, true));
   T2VA_TRY(check_scalar_out(status, false));
-  NoiseArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.B = batch;
-  a.M = num_modalities;
-  a.t = t;
-  a.status = status;
-  const int VE = dtype == T2VA_BFLOAT16 ? 8 : 4;
-  const int64_t per_cta = noise_vectors_per_cta();
-  int64_t total = 0;
-  for (int m = 0; m < num_modalities; ++m) {
-    a.n[m] = seg[m].numel;
-    a.stride[m] = seg[m].sample_stride;
-    a.z0[m] = z0[m];
-    a.eps[m] = eps[m];
-    a.zt[m] = zt[m];
-    // CTAs per (sample, modality); an empty modality gets no CTA at all
-    const int64_t vec_ub = (seg[m].numel + VE - 1) / VE;
-    const int64_t chunks = (vec_ub + per_cta - 1) / per_cta;
-    if (chunks > INT32_MAX) return T2VA_ERROR_INVALID_ARGUMENT;
-    a.chunks[m] = chunks > 0 ? (int)chunks : 1;
-    a.block_off[m] = (int)total;
-    total += (int64_t)batch * chunks;
-    if (total > INT32_MAX) return T2VA_ERROR_INVALID_ARGUMENT;
-  }
-  for (int m = num_modalities; m <= kMaxM; ++m) {
-    if (m < kMaxM) a.chunks[m] = 1;
-    a.block_off[m] = (int)total;
-  }
-  if (total == 0) return T2VA_SUCCESS;
-  if (launch_noise(a, dtype, (int)total, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return T2VA_ERROR_CUDA;
-  }
-  return T2VA_SUCCESS;
+  return run_noise(batch, num_modalities, seg, dtype, z0, eps, zt, nullptr, t, nullptr, status,
+                   kNoiseZt, stream);
+}
+
+int t2va_noise_rf(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+                  const void* const* z0, const void* const* eps, void* const* zt,
+                  void* const* z_rf, const float* t, float* t_rf, int* status,
+                  cudaStream_t stream) {
+  T2VA_TRY(check_geometry(batch, num_modalities, seg));
+  T2VA_TRY(check_dtype(dtype));
+  if (batch == 0) return T2VA_SUCCESS;
+  T2VA_TRY(check_ptrs(num_modalities, seg, z0));
+  T2VA_TRY(check_ptrs(num_modalities, seg, eps));
+  if (zt != nullptr)
+    T2VA_TRY(check_ptrs(num_modalities, seg, reinterpret_cast<const void* const*>(zt)));
+  T2VA_TRY(check_ptrs(num_modalities, seg, reinterpret_cast<const void* const*>(z_rf)));
+  for (int m = 0; zt != nullptr && m < num_modalities; ++m)
+    if (seg[m].numel > 0 && zt[m] == z_rf[m]) return T2VA_ERROR_INVALID_ARGUMENT;
+  T2VA_TRY(check_scalar_out(t, true));
+  T2VA_TRY(check_scalar_out(t_rf, false));
+  T2VA_TRY(check_scalar_out(status, false));
+  return run_noise(batch, num_modalities, seg, dtype, z0, eps, zt, z_rf, t, t_rf, status,
+                   zt != nullptr ? (kNoiseZt | kNoiseRf) : kNoiseRf, stream);
 }
 
 int t2va_scm_objective(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
@@ -315,53 +425,29 @@ int t2va_stage3_objective(int batch, int num_modalities, const t2va_segment* seg
                           float* loss, float* loss_scm, float* loss_dmd, float* norm, float* cdmd,
                           void* workspace, size_t workspace_bytes, int* status,
                           cudaStream_t stream) {
-  const int M = num_modalities;
-  T2VA_TRY(check_geometry(batch, M, seg));
-  T2VA_TRY(check_dtype(dtype));
-  if (batch == 0) return T2VA_SUCCESS;
-  for (const void* const* p : {z_t, x0_teacher, x0_student, x0_student_tangent, zhat0,
-                               x0_teacher_hat, x0_fake})
-    T2VA_TRY(check_ptrs(M, seg, p));
-  T2VA_TRY(check_ptrs(M, seg, reinterpret_cast<const void* const*>(grad_x0_student)));
-  T2VA_TRY(check_ptrs(M, seg, reinterpret_cast<const void* const*>(grad_zhat0)));
-  T2VA_TRY(check_scalar_out(t, true));
-  T2VA_TRY(check_scalar_out(loss, true));
-  for (const float* p : {loss_scm, loss_dmd, norm, cdmd}) T2VA_TRY(check_scalar_out(p, false));
-  T2VA_TRY(check_scalar_out(status, true));
-  T2VA_TRY(check_weights(M, weight));
-  if (!finite(beta) || !(gamma >= 0.f && gamma <= 1.f) || !finite(eps_scm) || !(eps_scm > 0.f) ||
-      !finite(lambda_scm) || !finite(eps_dmd) || !(eps_dmd > 0.f) || !finite(lambda_dmd))
-    return T2VA_ERROR_INVALID_ARGUMENT;
-  ObjectiveArgs a;
-  fill_geometry(a, batch, M, seg);
-  for (int m = 0; m < M; ++m) {
-    a.in[kZt][m] = z_t[m];
-    a.in[kXT][m] = x0_teacher[m];
-    a.in[kXS][m] = x0_student[m];
-    a.in[kXdot][m] = x0_student_tangent[m];
-    a.in[kZh][m] = zhat0[m];
-    a.in[kYT][m] = x0_teacher_hat[m];
-    a.in[kYF][m] = x0_fake[m];
-    a.grad_s[m] = grad_x0_student[m];
-    a.grad_d[m] = grad_zhat0[m];
-    if (grad_x0_student[m] == grad_zhat0[m]) a.alias_mask |= 1u << m;
-    a.w[m] = weight[m];
-  }
-  a.t = t;
-  a.beta = beta;
-  a.gamma = gamma;
-  a.eps_s = eps_scm;
-  a.lam_s = lambda_scm;
-  a.eps_d = eps_dmd;
-  a.lam_d = lambda_dmd;
-  a.accumulate = accumulate ? 1 : 0;
-  a.loss = loss;
-  a.loss_s = loss_scm;
-  a.loss_d = loss_dmd;
-  a.norm = norm;
-  a.cdmd = cdmd;
-  a.status = status;
-  return run_objective(a, dtype, kModeStage3, workspace, workspace_bytes, stream);
+  return stage3_impl(batch, num_modalities, seg, dtype, z_t, x0_teacher, x0_student,
+                     x0_student_tangent, t, zhat0, x0_teacher_hat, nullptr, nullptr, x0_fake, beta,
+                     gamma, eps_scm, eps_dmd, weight, lambda_scm, lambda_dmd, grad_x0_student,
+                     grad_zhat0, accumulate, loss, loss_scm, loss_dmd, norm, cdmd, workspace,
+                     workspace_bytes, status, stream);
+}
+
+int t2va_stage3_objective_cfg(
+    int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+    const void* const* z_t, const void* const* x0_teacher, const void* const* x0_student,
+    const void* const* x0_student_tangent, const float* t, const void* const* zhat0,
+    const void* const* x0_teacher_hat_cond, const void* const* x0_teacher_hat_uncond,
+    const float* guidance, const void* const* x0_fake, float beta, float gamma, float eps_scm,
+    float eps_dmd, const float* weight, float lambda_scm, float lambda_dmd,
+    float* const* grad_x0_student, float* const* grad_zhat0, int accumulate, float* loss,
+    float* loss_scm, float* loss_dmd, float* norm, float* cdmd, void* workspace,
+    size_t workspace_bytes, int* status, cudaStream_t stream) {
+  if (x0_teacher_hat_uncond == nullptr) return T2VA_ERROR_INVALID_ARGUMENT;
+  return stage3_impl(batch, num_modalities, seg, dtype, z_t, x0_teacher, x0_student,
+                     x0_student_tangent, t, zhat0, x0_teacher_hat_cond, x0_teacher_hat_uncond,
+                     guidance, x0_fake, beta, gamma, eps_scm, eps_dmd, weight, lambda_scm,
+                     lambda_dmd, grad_x0_student, grad_zhat0, accumulate, loss, loss_scm,
+                     loss_dmd, norm, cdmd, workspace, workspace_bytes, status, stream);
 }
 
 }  // extern "C"

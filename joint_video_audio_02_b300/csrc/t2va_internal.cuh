@@ -39,10 +39,13 @@ inline size_t ws_bytes(int B, int M, int /*sm_count*/) {
 }
 
 // Modes of the objective kernel.
-enum : int { kModeScm = 1, kModeDmd = 2, kModeStage3 = 3 };
+enum : int { kModeScm = 1, kModeDmd = 2, kModeStage3 = 3, kModeCfg = 4 };
 
 // Input tensor slots of the objective kernel.
-enum : int { kZt = 0, kXT = 1, kXS = 2, kXdot = 3, kZh = 4, kYT = 5, kYF = 6, kNumInputs = 7 };
+// With kModeCfg, slot kYT holds the teacher's conditional prediction at the re-noised
+// sample and kYU its unconditional one; the guided prediction is formed per element.
+enum : int { kZt = 0, kXT = 1, kXS = 2, kXdot = 3, kZh = 4, kYT = 5, kYF = 6, kYU = 7,
+             kNumInputs = 8 };
 
 struct ObjectiveArgs {
   int B, M;
@@ -54,6 +57,7 @@ struct ObjectiveArgs {
   const float* t;
   float beta, gamma, eps_s, lam_s, eps_d, lam_d;
   float w[kMaxM];
+  float cfg[kMaxM];            // guidance scale per modality (kModeCfg)
   int accumulate;
   uint32_t alias_mask;         // bit m: grad_d[m] == grad_s[m], write the sum once
   uint32_t wide_mask;          // bit m: the gradient buffers of m are 32-byte aligned
@@ -77,15 +81,21 @@ struct NoiseArgs {
   int64_t stride[kMaxM];
   const void* z0[kMaxM];
   const void* eps[kMaxM];
-  void* zt[kMaxM];
+  void* zt[kMaxM];             // TrigFlow sample (when the launch writes it)
+  void* zrf[kMaxM];            // rectified-flow sample (when the launch writes it)
   int chunks[kMaxM];           // CTAs per (sample, modality)
-  int block_off[kMaxM + 1];    // first CTA of each modality
+  int block_off[kMaxM + 1];    // first CTA of each modality; block_off[M] = element CTAs
   const float* t;
+  float* t_rf;                 // rectified-flow time per sample, or null
   int* status;
 };
 
+// Outputs of a noising launch.
+enum NoiseOut : int { kNoiseZt = 1, kNoiseRf = 2 };
+
 // Launchers (defined next to their kernels). They return a cudaError_t.
-cudaError_t launch_noise(const NoiseArgs& a, t2va_dtype dt, int grid, cudaStream_t st);
+// `grid` is at least a.block_off[a.M], and at least a.B when a.t_rf is set.
+cudaError_t launch_noise(const NoiseArgs& a, t2va_dtype dt, int outputs, int grid, cudaStream_t st);
 int noise_vectors_per_cta();
 
 struct ObjectiveLaunch {

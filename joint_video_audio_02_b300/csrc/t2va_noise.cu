@@ -1,13 +1,17 @@
 // TrigFlow noising kernel: z_t = cos(t) z0 + sin(t) eps per modality, with one
 // timestep per sample shared by all modalities (TurboT2VA, section 三 of the
 // robotworld.top/zh reading: the noising equation; section 2 of the
-// robotworld.top/en summary).
+// robotworld.top/en summary), fused with the TrigFlow -> rectified-flow wrapper
+// (section 4.2 of the zh reading; Eq. 16 of the en summary): z_rf = z_t / (cos t +
+// sin t) and t_rf = sin t / (cos t + sin t).
 //
-// HBM-bound stream: 2 reads + 1 write per element. Each CTA owns one chunk of
-// one (sample, modality) segment, so the per-sample sin/cos is computed once per
+// HBM-bound stream: 2 reads and 1 or 2 writes per element. Each CTA owns one chunk
+// of one (sample, modality) segment, so the per-sample sin/cos is computed once per
 // thread and every access is a coalesced 16-byte vector; the few elements before
 // the first 16-byte boundary and after the last full vector of a segment are
-// done one by one by the first and last chunk.
+// done one by one by the first and last chunk. Both outputs come from the same
+// loaded z0 and eps, each with one fma of float32 coefficients: cos t, sin t for
+// z_t, and cos t / (cos t + sin t), sin t / (cos t + sin t) for z_rf.
 #include "t2va_internal.cuh"
 
 namespace t2va {
@@ -54,10 +58,29 @@ __device__ __forceinline__ void store_scalar<__nv_bfloat16>(void* base, int64_t 
   reinterpret_cast<__nv_bfloat16*>(base)[e] = __float2bfloat16_rn(v);
 }
 
-template <typename T>
+// One output element from the loaded pair and the output's two coefficients.
+__device__ __forceinline__ float mix(float cz, float z, float ce, float e) {
+  return fmaf(cz, z, ce * e);
+}
+
+template <typename T, int OUT>
 __global__ void __launch_bounds__(kNoiseThreads) k_noise(const __grid_constant__ NoiseArgs a) {
   constexpr int VE = Vec<T>::VE;
   const int bid = blockIdx.x;
+
+  // launched as a programmatic dependent of the previous kernel on the stream: no
+  // memory access before that kernel has finished
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  // the rectified-flow time of sample `bid`, by CTA `bid` (the grid has at least B CTAs)
+  if ((OUT & kNoiseRf) && a.t_rf != nullptr && bid < a.B && threadIdx.x == 0) {
+    float s, c;
+    sincosf(__ldg(a.t + bid), &s, &c);
+    a.t_rf[bid] = s / (c + s);
+  }
+  if (bid >= a.block_off[a.M]) return;  // a CTA only there for t_rf
+
   int m = 0;
 #pragma unroll
   for (int i = 1; i < kMaxM; ++i)
@@ -66,21 +89,23 @@ __global__ void __launch_bounds__(kNoiseThreads) k_noise(const __grid_constant__
   const int b = local / a.chunks[m];
   const int chunk = local - b * a.chunks[m];
 
-  // launched as a programmatic dependent of the previous kernel on the stream: no
-  // memory access before that kernel has finished
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
   const float t = __ldg(a.t + b);
   float s, c;
   sincosf(t, &s, &c);
   if (!isfinite(t) && a.status != nullptr && threadIdx.x == 0 && chunk == 0)
     atomicOr(a.status, T2VA_STATUS_BAD_TIMESTEP);
+  float cr = 0.f, sr = 0.f;
+  if (OUT & kNoiseRf) {
+    cr = c / (c + s);
+    sr = s / (c + s);
+  }
 
   const SegGeom g = seg_geom<VE>(a.n[m], a.stride[m], b);
   const int64_t vec0 = g.e0 + g.head;  // element index of vector 0
   const T* z0 = reinterpret_cast<const T*>(a.z0[m]);
   const T* ep = reinterpret_cast<const T*>(a.eps[m]);
   T* zt = reinterpret_cast<T*>(a.zt[m]);
+  T* zr = reinterpret_cast<T*>(a.zrf[m]);
 
   const int64_t vbeg = (int64_t)chunk * kNoiseVecPerCta;
   uint4 rz[kNoiseUnroll], re[kNoiseUnroll];
@@ -100,19 +125,31 @@ __global__ void __launch_bounds__(kNoiseThreads) k_noise(const __grid_constant__
       vz.from(rz[u]);
       ve.from(re[u]);
       float o[VE];
+      if (OUT & kNoiseZt) {
 #pragma unroll
-      for (int k = 0; k < VE; ++k) o[k] = fmaf(c, vz.v[k], s * ve.v[k]);
-      store_vec<T>(zt + vec0 + v * VE, o);
+        for (int k = 0; k < VE; ++k) o[k] = mix(c, vz.v[k], s, ve.v[k]);
+        store_vec<T>(zt + vec0 + v * VE, o);
+      }
+      if (OUT & kNoiseRf) {
+#pragma unroll
+        for (int k = 0; k < VE; ++k) o[k] = mix(cr, vz.v[k], sr, ve.v[k]);
+        store_vec<T>(zr + vec0 + v * VE, o);
+      }
     }
   }
-  // unaligned head (first chunk) and tail (last chunk): one element per thread
-  if (chunk == 0 && threadIdx.x < g.head) {
-    const int64_t e = g.e0 + threadIdx.x;
-    store_scalar<T>(zt, e, fmaf(c, load_scalar<T>(z0, e), s * load_scalar<T>(ep, e)));
-  }
-  if (chunk == a.chunks[m] - 1 && threadIdx.x < g.tail) {
-    const int64_t e = vec0 + g.nvec * VE + threadIdx.x;
-    store_scalar<T>(zt, e, fmaf(c, load_scalar<T>(z0, e), s * load_scalar<T>(ep, e)));
+  // unaligned head (first chunk) and tail (last chunk): one element per thread each
+  // (a one-chunk segment's thread may have one of both)
+#pragma unroll
+  for (int side = 0; side < 2; ++side) {
+    int64_t e = -1;
+    if (side == 0 && chunk == 0 && threadIdx.x < g.head) e = g.e0 + threadIdx.x;
+    if (side == 1 && chunk == a.chunks[m] - 1 && threadIdx.x < g.tail)
+      e = vec0 + g.nvec * VE + threadIdx.x;
+    if (e >= 0) {
+      const float z = load_scalar<T>(z0, e), x = load_scalar<T>(ep, e);
+      if (OUT & kNoiseZt) store_scalar<T>(zt, e, mix(c, z, s, x));
+      if (OUT & kNoiseRf) store_scalar<T>(zr, e, mix(cr, z, sr, x));
+    }
   }
 }
 
@@ -120,7 +157,8 @@ __global__ void __launch_bounds__(kNoiseThreads) k_noise(const __grid_constant__
 
 int noise_vectors_per_cta() { return kNoiseVecPerCta; }
 
-cudaError_t launch_noise(const NoiseArgs& a, t2va_dtype dt, int grid, cudaStream_t st) {
+cudaError_t launch_noise(const NoiseArgs& a, t2va_dtype dt, int outputs, int grid,
+                         cudaStream_t st) {
   // a programmatic dependent of the previous work on the stream (see k_noise)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -131,8 +169,20 @@ cudaError_t launch_noise(const NoiseArgs& a, t2va_dtype dt, int grid, cudaStream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (dt == T2VA_BFLOAT16) return cudaLaunchKernelEx(&cfg, k_noise<__nv_bfloat16>, a);
-  return cudaLaunchKernelEx(&cfg, k_noise<float>, a);
+  const bool bf = dt == T2VA_BFLOAT16;
+  switch (outputs) {
+    case kNoiseZt:
+      return bf ? cudaLaunchKernelEx(&cfg, k_noise<__nv_bfloat16, kNoiseZt>, a)
+                : cudaLaunchKernelEx(&cfg, k_noise<float, kNoiseZt>, a);
+    case kNoiseRf:
+      return bf ? cudaLaunchKernelEx(&cfg, k_noise<__nv_bfloat16, kNoiseRf>, a)
+                : cudaLaunchKernelEx(&cfg, k_noise<float, kNoiseRf>, a);
+    case kNoiseZt | kNoiseRf:
+      return bf ? cudaLaunchKernelEx(&cfg, k_noise<__nv_bfloat16, kNoiseZt | kNoiseRf>, a)
+                : cudaLaunchKernelEx(&cfg, k_noise<float, kNoiseZt | kNoiseRf>, a);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace t2va

@@ -40,12 +40,25 @@ struct Traits {
   static constexpr int VE = Vec<T>::VE;
   static constexpr bool kScm = (MODE & kModeScm) != 0;
   static constexpr bool kDmd = (MODE & kModeDmd) != 0;
+  static constexpr bool kCfg = kDmd && (MODE & kModeCfg) != 0;
   static constexpr int k0 = kScm ? kZt : kZh;  // first input slot of the mode
-  static constexpr int NIN = (kScm ? 4 : 0) + (kDmd ? 3 : 0);
+  static constexpr int NIN = (kScm ? 4 : 0) + (kDmd ? 3 : 0) + (kCfg ? 1 : 0);
   // the gradient pass needs no zhat0 (it enters only the residual scale)
-  static constexpr int NG = (kScm ? 4 : 0) + (kDmd ? 2 : 0);
+  static constexpr int NG = (kScm ? 4 : 0) + (kDmd ? 2 : 0) + (kCfg ? 1 : 0);
   static constexpr int kYT0 = kScm ? 4 : 0;  // position of y_T among the gradient inputs
+  // resident gradient-pass CTAs per SM: three, or two for the seven inputs of the
+  // guided stage-3 pass (three would cap the registers below its in-flight loads)
+  static constexpr int kGradCtas = (kScm && kCfg) ? 2 : 3;
 };
+
+// The teacher prediction at the re-noised sample: the stored one, or with guidance
+// the unconditional prediction moved s times the way to the conditional one,
+// u + s (k - u), in float32 with one fma.
+template <bool CFG>
+__device__ __forceinline__ float teacher(float k, float u, float s) {
+  if constexpr (CFG) return fmaf(s, k - u, u);
+  return k;
+}
 
 // ---------------------------------------------------------------------------
 // loads, cache policies, reductions
@@ -152,15 +165,17 @@ __device__ __forceinline__ int64_t edge_element(const ObjectiveArgs& a, const Ch
 struct Coefs {
   float kD, kz, kx, s;
   bool ok;
+  float cfg;  // guidance scale of the row's modality (kModeCfg)
 };
 
 template <typename T, int MODE>
-__device__ __forceinline__ Coefs coefs_of(const ObjectiveArgs& a, int b) {
-  Coefs c{0.f, 0.f, 0.f, 1.f, true};
+__device__ __forceinline__ Coefs coefs_of(const ObjectiveArgs& a, int b, int m) {
+  Coefs c{0.f, 0.f, 0.f, 1.f, true, 1.f};
   if constexpr (Traits<T, MODE>::kScm) {
     const Coef k = sample_coef(__ldg(a.t + b), a.beta, a.gamma);
-    c = Coefs{k.kD, k.kz, k.kx, k.s, k.ok};
+    c = Coefs{k.kD, k.kz, k.kx, k.s, k.ok, 1.f};
   }
+  if constexpr (Traits<T, MODE>::kCfg) c.cfg = a.cfg[m];
   return c;
 }
 
@@ -194,16 +209,18 @@ __device__ __forceinline__ void directions(const uint4 (&in)[Traits<T, MODE>::NI
     }
   }
   if constexpr (Tr::kDmd) {
-    Vec<T> zh, yt, yf;
+    Vec<T> zh, yt, yf, yu;
     zh.from(in[kZh - Tr::k0]);
     yt.from(in[kYT - Tr::k0]);
     yf.from(in[kYF - Tr::k0]);
+    if constexpr (Tr::kCfg) yu.from(in[kYU - Tr::k0]);
 #pragma unroll
     for (int i = 0; i < VE; ++i) {
-      const float g = yf.v[i] - yt.v[i];
+      const float y = teacher<Tr::kCfg>(yt.v[i], Tr::kCfg ? yu.v[i] : 0.f, k.cfg);
+      const float g = yf.v[i] - y;
       gd[i] = g;
       sd = fmaf(g, g, sd);
-      sa += fabsf(zh.v[i] - yt.v[i]);
+      sa += fabsf(zh.v[i] - y);
     }
   }
 }
@@ -221,6 +238,8 @@ __device__ __forceinline__ void load_grad_vec(uint4 (&in)[Traits<T, MODE>::NG], 
     in[Tr::kYT0] = ld16(reinterpret_cast<const T*>(a.in[kYT][m]) + e, policy);
     in[Tr::kYT0 + 1] = ld16(reinterpret_cast<const T*>(a.in[kYF][m]) + e, policy);
   }
+  if constexpr (Tr::kCfg)
+    in[Tr::kYT0 + 2] = ld16(reinterpret_cast<const T*>(a.in[kYU][m]) + e, policy);
 }
 
 // The unscaled directions of one vector from the gradient pass's inputs.
@@ -240,11 +259,13 @@ __device__ __forceinline__ void grad_directions(const uint4 (&in)[Traits<T, MODE
       gs[i] = fmaf(k.kD, xt.v[i] - xs.v[i], fmaf(k.kz, z.v[i], k.kx * xd.v[i]));
   }
   if constexpr (Tr::kDmd) {
-    Vec<T> yt, yf;
+    Vec<T> yt, yf, yu;
     yt.from(in[Tr::kYT0]);
     yf.from(in[Tr::kYT0 + 1]);
+    if constexpr (Tr::kCfg) yu.from(in[Tr::kYT0 + 2]);
 #pragma unroll
-    for (int i = 0; i < VE; ++i) gd[i] = yf.v[i] - yt.v[i];
+    for (int i = 0; i < VE; ++i)
+      gd[i] = yf.v[i] - teacher<Tr::kCfg>(yt.v[i], Tr::kCfg ? yu.v[i] : 0.f, k.cfg);
   }
 }
 
@@ -262,7 +283,8 @@ __device__ __forceinline__ void scalar_direction(const ObjectiveArgs& a, int m, 
   }
   if constexpr (Tr::kDmd) {
     const float zh = load_scalar<T>(a.in[kZh][m], e);
-    const float yt = load_scalar<T>(a.in[kYT][m], e);
+    const float yu = Tr::kCfg ? load_scalar<T>(a.in[kYU][m], e) : 0.f;
+    const float yt = teacher<Tr::kCfg>(load_scalar<T>(a.in[kYT][m], e), yu, k.cfg);
     const float yf = load_scalar<T>(a.in[kYF][m], e);
     gd = yf - yt;
     sabs = fabsf(zh - yt);
@@ -352,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_sums(const __grid_constant__ Ob
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const Chunk k = chunk_of<VE>(a, blockIdx.x);
-  const Coefs cf = coefs_of<T, MODE>(a, k.b);
+  const Coefs cf = coefs_of<T, MODE>(a, k.b, k.m);
   const uint64_t keep = policy_evict_last();
   float sg = 0.f, sa = 0.f, sd = 0.f;
   for (int64_t base = k.v_lo; base < k.v_hi; base += kBatchVec) {
@@ -404,12 +426,13 @@ __device__ __forceinline__ float3 row_totals(const ObjectiveArgs& a, int b, int 
 }
 
 template <typename T, int MODE>
-__global__ void __launch_bounds__(kThreads, 3) k_grads(const __grid_constant__ ObjectiveArgs a) {
+__global__ void __launch_bounds__(kThreads, Traits<T, MODE>::kGradCtas)
+    k_grads(const __grid_constant__ ObjectiveArgs a) {
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
   __shared__ float3 scratch[kWarps];
   const Chunk k = chunk_of<VE>(a, blockIdx.x);
-  const Coefs cf = coefs_of<T, MODE>(a, k.b);
+  const Coefs cf = coefs_of<T, MODE>(a, k.b, k.m);
   const uint64_t drop = policy_evict_first();
   const float qnan = __int_as_float(0x7fc00000);
 
@@ -581,13 +604,16 @@ bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int /*mode*/, int sm_count,
 
 cudaError_t launch_objective(const ObjectiveArgs& a, t2va_dtype dt, int mode,
                              const ObjectiveLaunch& l, cudaStream_t st) {
+  constexpr int kCfg3 = kModeStage3 | kModeCfg;
   if (dt == T2VA_BFLOAT16) {
     if (mode == kModeScm) return launch_t<__nv_bfloat16, kModeScm>(a, l, st);
     if (mode == kModeDmd) return launch_t<__nv_bfloat16, kModeDmd>(a, l, st);
+    if (mode == kCfg3) return launch_t<__nv_bfloat16, kCfg3>(a, l, st);
     return launch_t<__nv_bfloat16, kModeStage3>(a, l, st);
   }
   if (mode == kModeScm) return launch_t<float, kModeScm>(a, l, st);
   if (mode == kModeDmd) return launch_t<float, kModeDmd>(a, l, st);
+  if (mode == kCfg3) return launch_t<float, kCfg3>(a, l, st);
   return launch_t<float, kModeStage3>(a, l, st);
 }
 

@@ -10,6 +10,7 @@ from .workloads import (  # noqa: F401
     DMD,
     SCM,
     STAGE3,
+    STAGE3_CFG,
     WORKLOADS,
     Inputs,
     Workload,

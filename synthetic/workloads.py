@@ -14,7 +14,11 @@ for every workload:
   fresh noise eps' ~ N(0, 1); teacher prediction at the re-noised sample
   y_T = zhat0 + 0.1 N; fake-score prediction y_fake = y_T + 0.1 N;
 * per-sample timestep t = arctan(exp(tau)), tau ~ N(-0.8, 1.6^2), clamped to
-  [1e-3, pi/2 - 1e-3] (fixed values for the tiny workload).
+  [1e-3, pi/2 - 1e-3] (fixed values for the tiny workload);
+* with a guided teacher (mode "stage3_cfg"), the stored teacher prediction above is
+  the conditional one and the unconditional one is u = y_T + 0.03 N, drawn after
+  every other input of the modality; the guidance scales are 3.0 for video and 5.0
+  for audio (TurboT2VA, section 七 training configuration).
 
 Values are drawn in float32 and stored either as float32 or as bfloat16 bit
 patterns (uint16, round-to-nearest-even). Nothing here computes any part of the
@@ -32,6 +36,7 @@ import numpy as np
 SCM = "scm"
 DMD = "dmd"
 STAGE3 = "stage3"
+STAGE3_CFG = "stage3_cfg"
 
 
 @dataclasses.dataclass(frozen=True)
@@ -40,7 +45,7 @@ class Workload:
     batch: int
     shapes: tuple          # per modality, the per-sample latent shape
     dtype: str             # "f32" or "bf16"
-    mode: str              # "scm", "dmd" or "stage3"
+    mode: str              # "scm", "dmd", "stage3" or "stage3_cfg"
     seed: tuple
     beta: float = 1.0
     gamma: float = 0.9
@@ -50,6 +55,8 @@ class Workload:
     lambda_dmd: float = 0.25
     eps_dmd: float = 1e-6
     t_fixed: Optional[tuple] = None
+    guidance: tuple = (3.0, 5.0)  # per modality, for "stage3_cfg"
+    rf_wrapper: bool = False      # noising also writes the rectified-flow latents and times
     description: str = ""
 
     @property
@@ -90,6 +97,15 @@ for _wl in [
        mode=STAGE3, seed=(4, b), weight=(1.0, 4.0),
        description=f"batch/modality-imbalance sweep, B={b}, audio 504x128, w=(1,4)")
     for b in (1, 4, 16, 32)
+] + [
+    _w("stage3_cfg_512x768_bf16", batch=4, shapes=(VIDEO_512x768, AUDIO_126), dtype="bf16",
+       mode=STAGE3_CFG, seed=(5,), description="512x768 shape, sCM+DMD with a guided teacher"),
+    _w("stage3_cfg_1024x1792_bf16", batch=1, shapes=(VIDEO_1024x1792, AUDIO_126), dtype="bf16",
+       mode=STAGE3_CFG, seed=(6,), description="1024x1792 shape, sCM+DMD with a guided teacher"),
+    _w("stage3_cfg_rf_512x768_bf16", batch=4, shapes=(VIDEO_512x768, AUDIO_126), dtype="bf16",
+       mode=STAGE3_CFG, seed=(7,), rf_wrapper=True,
+       description="512x768 shape, noising with the rectified-flow wrapper, sCM+DMD with a "
+                   "guided teacher"),
 ]:
     WORKLOADS[_wl.name] = _wl
 
@@ -137,6 +153,7 @@ class Inputs:
     eps_hat: List[np.ndarray] = None
     x0_teacher_hat: List[np.ndarray] = None
     x0_fake: List[np.ndarray] = None
+    x0_teacher_hat_uncond: List[np.ndarray] = None
 
     @property
     def batch(self) -> int:
@@ -171,23 +188,27 @@ def make_inputs(batch: int, numels: Sequence[int], dtype: str, mode: str, seed,
         return a
 
     out = Inputs(dtype=dtype, mode=mode, t=tt, z0=[], eps=[])
-    if mode in (SCM, STAGE3):
+    scm = mode in (SCM, STAGE3, STAGE3_CFG)
+    dmd = mode in (DMD, STAGE3, STAGE3_CFG)
+    if scm:
         out.x0_teacher, out.x0_student, out.x0_tangent = [], [], []
-    if mode in (DMD, STAGE3):
+    if dmd:
         out.zhat0, out.eps_hat, out.x0_teacher_hat, out.x0_fake = [], [], [], []
+    if mode == STAGE3_CFG:
+        out.x0_teacher_hat_uncond = []
     for n in numels:
         z0 = normal(n)
         eps = normal(n)
         out.z0.append(_store(z0, dtype))
         out.eps.append(_store(eps, dtype))
-        if mode in (SCM, STAGE3):
+        if scm:
             xt = z0 + normal(n, 0.1)
             xs = xt + normal(n, 0.05)
             out.x0_teacher.append(_store(xt, dtype))
             out.x0_student.append(_store(xs, dtype))
             out.x0_tangent.append(_store(normal(n, 0.5), dtype))
             del xt, xs
-        if mode in (DMD, STAGE3):
+        if dmd:
             zh = normal(n) + normal(n, 0.1) + normal(n, 0.05)
             eh = normal(n)
             yt = zh + normal(n, 0.1)
@@ -196,6 +217,8 @@ def make_inputs(batch: int, numels: Sequence[int], dtype: str, mode: str, seed,
             out.eps_hat.append(_store(eh, dtype))
             out.x0_teacher_hat.append(_store(yt, dtype))
             out.x0_fake.append(_store(yf, dtype))
+            if mode == STAGE3_CFG:
+                out.x0_teacher_hat_uncond.append(_store(yt + normal(n, 0.03), dtype))
             del zh, eh, yt, yf
         del z0, eps
     return out
@@ -214,6 +237,8 @@ def slice_samples(inp: Inputs, samples: Sequence[int]) -> Inputs:
         v = getattr(inp, f.name)
         if isinstance(v, list):
             kw[f.name] = [a[idx] for a in v]
+        elif v is None:
+            kw[f.name] = None
         elif f.name == "t":
             kw[f.name] = v[idx]
         else:

@@ -22,6 +22,9 @@ import synthetic as S
 
 RTOL = {"f32": 1e-5, "bf16": 1e-4}
 GRAD_FRAC = 1e-3
+STAGE3_MODES = (S.STAGE3, S.STAGE3_CFG)
+SCM_MODES = (S.SCM,) + STAGE3_MODES
+DMD_MODES = (S.DMD,) + STAGE3_MODES
 
 
 def to_device(arrs: Sequence[np.ndarray], dtype: str, stride_pad: int = 0) -> List[torch.Tensor]:
@@ -75,10 +78,12 @@ class Params:
     weight: tuple = (1.0, 1.0)
     lambda_scm: float = 1.0
     lambda_dmd: float = 0.25
+    guidance: tuple = (3.0, 5.0)
 
     @staticmethod
     def of(wl: S.Workload) -> "Params":
-        return Params(wl.beta, wl.gamma, wl.eps_scm, wl.eps_dmd, tuple(wl.weight), wl.lambda_scm, wl.lambda_dmd)
+        return Params(wl.beta, wl.gamma, wl.eps_scm, wl.eps_dmd, tuple(wl.weight), wl.lambda_scm,
+                      wl.lambda_dmd, tuple(wl.guidance))
 
 
 def gpu_run(inp: S.Inputs, p: Params, mode: str, stride_pad: int = 0, accumulate_into=None,
@@ -94,7 +99,7 @@ def gpu_run(inp: S.Inputs, p: Params, mode: str, stride_pad: int = 0, accumulate
     loss = torch.full((B,), float("nan"), device="cuda")
     norm = torch.full((B * M,), float("nan"), device="cuda")
     cdmd = torch.full((B * M,), float("nan"), device="cuda")
-    if mode in (S.SCM, S.STAGE3):
+    if mode in SCM_MODES:
         z0 = to_device(inp.z0, dt, stride_pad)
         eps = to_device(inp.eps, dt, stride_pad)
         zt = alloc_like(z0)
@@ -107,7 +112,7 @@ def gpu_run(inp: S.Inputs, p: Params, mode: str, stride_pad: int = 0, accumulate
             for g, a in zip(gS, accumulate_into["grad_x0_student"]):
                 g.copy_(torch.from_numpy(np.asarray(a, np.float32)))
         out["zt"] = to_host(zt, dt)
-    if mode in (S.DMD, S.STAGE3):
+    if mode in DMD_MODES:
         zh = to_device(inp.zhat0, dt, stride_pad)
         yT = to_device(inp.x0_teacher_hat, dt, stride_pad)
         yF = to_device(inp.x0_fake, dt, stride_pad)
@@ -115,6 +120,8 @@ def gpu_run(inp: S.Inputs, p: Params, mode: str, stride_pad: int = 0, accumulate
         if accumulate_into is not None:
             for g, a in zip(gD, accumulate_into["grad_zhat0"]):
                 g.copy_(torch.from_numpy(np.asarray(a, np.float32)))
+    if mode == S.STAGE3_CFG:
+        yU = to_device(inp.x0_teacher_hat_uncond, dt, stride_pad)
     acc = accumulate_into is not None
     if mode == S.SCM:
         t2va.scm_objective(zt, xT, xS, tan, t, beta=p.beta, gamma=p.gamma, eps_scm=p.eps_scm,
@@ -129,21 +136,25 @@ def gpu_run(inp: S.Inputs, p: Params, mode: str, stride_pad: int = 0, accumulate
         loss_d = torch.full((B,), float("nan"), device="cuda")
         if alias:
             gD = gS
-        t2va.stage3_objective(zt, xT, xS, tan, t, zh, yT, yF, beta=p.beta, gamma=p.gamma,
-                              eps_scm=p.eps_scm, eps_dmd=p.eps_dmd, weight=p.weight,
-                              lambda_scm=p.lambda_scm, lambda_dmd=p.lambda_dmd,
-                              grad_x0_student=gS, grad_zhat0=gD, loss=loss, loss_scm=loss_s,
-                              loss_dmd=loss_d, norm=norm, cdmd=cdmd, accumulate=acc,
-                              workspace=ws, status=status)
+        common = dict(beta=p.beta, gamma=p.gamma, eps_scm=p.eps_scm, eps_dmd=p.eps_dmd,
+                      weight=p.weight, lambda_scm=p.lambda_scm, lambda_dmd=p.lambda_dmd,
+                      grad_x0_student=gS, grad_zhat0=gD, loss=loss, loss_scm=loss_s,
+                      loss_dmd=loss_d, norm=norm, cdmd=cdmd, accumulate=acc, workspace=ws,
+                      status=status)
+        if mode == S.STAGE3_CFG:
+            t2va.stage3_objective_cfg(zt, xT, xS, tan, t, zh, yT, yU, yF, guidance=p.guidance,
+                                      **common)
+        else:
+            t2va.stage3_objective(zt, xT, xS, tan, t, zh, yT, yF, **common)
         out["loss_scm"] = loss_s.cpu().numpy()
         out["loss_dmd"] = loss_d.cpu().numpy()
     torch.cuda.synchronize()
     out["loss"] = loss.cpu().numpy()
     out["norm"] = norm.cpu().numpy().reshape(B, M)
     out["cdmd"] = cdmd.cpu().numpy().reshape(B, M)
-    if mode in (S.SCM, S.STAGE3):
+    if mode in SCM_MODES:
         out["grad_x0_student"] = [g.contiguous().cpu().numpy() for g in gS]
-    if mode in (S.DMD, S.STAGE3):
+    if mode in DMD_MODES:
         out["grad_zhat0"] = [g.contiguous().cpu().numpy() for g in gD]
     out["status"] = int(status.item())
     return out
@@ -153,7 +164,7 @@ def oracle_run(inp: S.Inputs, p: Params, mode: str, t_override=None):
     dt = inp.dtype
     t = np.asarray(t_override if t_override is not None else inp.t, np.float32)
     out = {}
-    if mode in (S.SCM, S.STAGE3):
+    if mode in SCM_MODES:
         zt = oracle.noise(inp.z0, inp.eps, t, dt)
         out["zt"] = zt
     if mode == S.SCM:
@@ -162,6 +173,11 @@ def oracle_run(inp: S.Inputs, p: Params, mode: str, t_override=None):
     elif mode == S.DMD:
         r = oracle.dmd_objective(inp.zhat0, inp.x0_teacher_hat, inp.x0_fake, p.eps_dmd, p.weight,
                                  p.lambda_dmd, dt)
+    elif mode == S.STAGE3_CFG:
+        r = oracle.stage3_objective_cfg(zt, inp.x0_teacher, inp.x0_student, inp.x0_tangent, t,
+                                        inp.zhat0, inp.x0_teacher_hat, inp.x0_teacher_hat_uncond,
+                                        p.guidance, inp.x0_fake, p.beta, p.gamma, p.eps_scm,
+                                        p.eps_dmd, p.weight, p.lambda_scm, p.lambda_dmd, dt)
     else:
         r = oracle.stage3_objective(zt, inp.x0_teacher, inp.x0_student, inp.x0_tangent, t,
                                     inp.zhat0, inp.x0_teacher_hat, inp.x0_fake, p.beta, p.gamma,
@@ -231,14 +247,14 @@ def compare(gpu, ref, dtype: str, mode: str):
     rtol = RTOL[dtype]
     assert_rel(gpu["loss"], ref["loss"], rtol, "loss")
     M = gpu["norm"].shape[1]
-    if mode in (S.SCM, S.STAGE3):
+    if mode in SCM_MODES:
         assert_rel(gpu["norm"], ref["norm"], rtol, "norm")
         for m in range(M):
             assert_grad(gpu["grad_x0_student"][m], ref["grad_x0_student"][m], f"grad_x0_student[{m}]")
-    if mode in (S.DMD, S.STAGE3):
+    if mode in DMD_MODES:
         assert_rel(gpu["cdmd"], ref["cdmd"], rtol, "cdmd")
         for m in range(M):
             assert_grad(gpu["grad_zhat0"][m], ref["grad_zhat0"][m], f"grad_zhat0[{m}]")
-    if mode == S.STAGE3:
+    if mode in STAGE3_MODES:
         assert_rel(gpu["loss_scm"], ref["loss_scm"], rtol, "loss_scm")
         assert_rel(gpu["loss_dmd"], ref["loss_dmd"], rtol, "loss_dmd")

@@ -82,6 +82,22 @@ def test_host_validation_without_device(lib):
     assert lib.t2va_scm_objective(*args(1.0, 0.5, 1e-6, wbad)) == 1   # negative weight
     assert lib.t2va_dmd_objective(2, 2, segs, 1, ptrs, ptrs, ptrs, -1.0, w, 1.0, ptrs, 0, ok, None,
                                   ok, 1 << 20, ok, None) == 1
+    # the fused RF noising: z_rf required, z_t optional but never the z_rf buffer
+    assert lib.t2va_noise_rf(2, 2, segs, 1, ptrs, ptrs, None, None, ok, None, None, None) == 1
+    assert lib.t2va_noise_rf(2, 2, segs, 1, ptrs, ptrs, ptrs, ptrs, ok, None, None, None) == 1
+    assert lib.t2va_noise_rf(2, 2, segs, 1, ptrs, ptrs, None, _p(ok + 8, ok), ok, None, None, None) == 3
+    assert lib.t2va_noise_rf(2, 2, segs, 1, ptrs, ptrs, None, ptrs, ok, ok + 2, None, None) == 3
+    assert lib.t2va_noise_rf(0, 2, segs, 1, ptrs, ptrs, None, ptrs, ok, None, None, None) == 0
+    # the guided stage-3 objective: the unconditional prediction and finite scales required
+    g_ok = (ctypes.c_float * 2)(3.0, 5.0)
+    g_bad = (ctypes.c_float * 2)(3.0, float("inf"))
+    cfg = lambda uncond, g: (2, 2, segs, 1, ptrs, ptrs, ptrs, ptrs, ok, ptrs, ptrs, uncond, g, ptrs,
+                             1.0, 0.5, 1e-6, 1e-6, w, 1.0, 1.0, ptrs, ptrs, 0, ok, None, None, None,
+                             None, ok, 1 << 20, ok, None)
+    assert lib.t2va_stage3_objective_cfg(*cfg(None, g_ok)) == 1
+    assert lib.t2va_stage3_objective_cfg(*cfg(ptrs, None)) == 1
+    assert lib.t2va_stage3_objective_cfg(*cfg(ptrs, g_bad)) == 1
+    assert lib.t2va_stage3_objective_cfg(*cfg(_p(ok + 8, ok), g_ok)) == 3
     # workspace checks come after the argument checks and need no device either
     assert lib.t2va_workspace_init(None, 1024, 0, None) == 4
     assert lib.t2va_workspace_init(ok + 4, 1024, 0, None) == 4
