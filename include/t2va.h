@@ -230,6 +230,40 @@ int t2va_stage3_objective_cfg(
     float* loss_scm, float* loss_dmd, float* norm, float* cdmd, void* workspace,
     size_t workspace_bytes, int* status, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Post-scale W8A8 linear  ([zh] 6.2; [en] section 6): static per-output-channel
+ * weight quantisation, dynamic per-row activation quantisation, an exact INT32
+ * sum over the whole K, and both scales applied once, after the sum:
+ *   s_i = max(||x_i||_inf, eps) / 127,  x_hat_i = clip(round(x_i / s_i), -127, 127),
+ *   y_ij = s_i^x s_j^w sum_k x_hat_ik w_hat_jk + b_j.
+ * --------------------------------------------------------------------------- */
+
+/* Quantise `rows` rows of `cols` elements (bfloat16 or float32, row i at
+ * x + i * ld_x elements) into int8 codes (row i at q + i * ld_q bytes) and float32
+ * scales scale[i] = max(amax_i, eps) / 127. Each code is rint(x / s) of the float32
+ * quotient (IEEE division, ties to even), clipped to [-127, 127], so codes are exact
+ * functions of the inputs. Use it for the activations before every linear and once
+ * for each weight matrix (rows = output channels). Requires eps > 0, cols a multiple
+ * of 16 bytes of input (8 bf16 or 4 float32 elements), ld_x * element size a
+ * multiple of 16, ld_q a multiple of 16 / element size, x and q 16-byte aligned.
+ * One warp per row: reads each input once (rows longer than 8 KiB are read a second
+ * time, from L2) and writes 1 byte per element. One kernel on `stream`. */
+int t2va_quantize_rows(int64_t rows, int64_t cols, t2va_dtype dtype, const void* x, int64_t ld_x,
+                       float eps, int8_t* q, int64_t ld_q, float* scale, cudaStream_t stream);
+
+/* y[M][N] (row-major, bfloat16 or float32 per `out_dtype`) from activation codes
+ * xq[M][K] with scales sx[M] and weight codes wq[N][K] with scales sw[N] (both
+ * K-contiguous), and an optional bias[N] (NULL for none). The integer sum is exact;
+ * the epilogue is y = fma(float(acc), sx_i * sw_j, b_j) in float32, rounded once to
+ * `out_dtype`. Shapes are guarded as in the paper: M, N and K must be multiples of
+ * 128 (else T2VA_ERROR_INVALID_ARGUMENT; the caller keeps its own BF16 linear for
+ * other shapes), and K <= 131072 so that no INT32 sum can overflow. sm_103a has no
+ * INT8 form of the fifth-generation tensor-core MMA, so the contraction runs on the
+ * warp-level INT8 MMA. One kernel on `stream`. */
+int t2va_w8a8_linear(int64_t M, int64_t N, int64_t K, const int8_t* xq, const float* sx,
+                     const int8_t* wq, const float* sw, const float* bias, t2va_dtype out_dtype,
+                     void* y, cudaStream_t stream);
+
 /* Bytes of the library's own scratch array used by
  * t2va_stage3_objective_noalloc (1 MiB). Every GPU that loads the library holds
  * this much device memory until the process exits. */

@@ -13,10 +13,12 @@ from .binding import (  # noqa: F401
     new_workspace,
     noise,
     noise_rf,
+    quantize_rows,
     scm_objective,
     stage3_objective,
     stage3_objective_cfg,
     stage3_objective_noalloc,
+    w8a8_linear,
     workspace_bytes,
     workspace_init,
 )

@@ -35,7 +35,8 @@ NOALLOC_SCRATCH_BYTES = 1 << 20   # T2VA_NOALLOC_SCRATCH_BYTES
 
 EXPORTED = ("t2va_error_string", "t2va_abi_version", "t2va_workspace_bytes", "t2va_workspace_init",
             "t2va_noise", "t2va_scm_objective", "t2va_dmd_objective", "t2va_stage3_objective",
-            "t2va_stage3_objective_noalloc", "t2va_noise_rf", "t2va_stage3_objective_cfg")
+            "t2va_stage3_objective_noalloc", "t2va_noise_rf", "t2va_stage3_objective_cfg",
+            "t2va_quantize_rows", "t2va_w8a8_linear")
 
 
 class Segment(ctypes.Structure):
@@ -85,6 +86,10 @@ def _declare(lib):
                                               c_float, c_float, c_float, c_float, P, c_float, c_float,
                                               P, P, c_int, P, P, P, P, P, P, c_size_t, P, P]
     lib.t2va_stage3_objective_cfg.restype = c_int
+    lib.t2va_quantize_rows.argtypes = [c_int64, c_int64, c_int, P, c_int64, c_float, P, c_int64, P, P]
+    lib.t2va_quantize_rows.restype = c_int
+    lib.t2va_w8a8_linear.argtypes = [c_int64, c_int64, c_int64, P, P, P, P, P, c_int, P, P]
+    lib.t2va_w8a8_linear.restype = c_int
 
 
 def load(path: Optional[str] = None):
@@ -291,6 +296,45 @@ def stage3_objective_cfg(z_t, x0_teacher, x0_student, x0_student_tangent, t, zha
         int(bool(accumulate)), loss.data_ptr(), _opt(loss_scm), _opt(loss_dmd), _opt(norm),
         _opt(cdmd), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         status.data_ptr(), _stream(stream)), "t2va_stage3_objective_cfg")
+
+
+W8A8_EPS = 1e-4
+
+
+def quantize_rows(x: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, eps: float = W8A8_EPS,
+                  stream=None):
+    """Per-row dynamic int8 quantisation of a 2-D CUDA tensor (t2va_quantize_rows): codes
+    into `q` (int8, same shape, rows 16-byte aligned) and scales into `scale` (float32)."""
+    if x.dim() != 2 or q.dim() != 2 or q.shape != x.shape or q.dtype != torch.int8:
+        raise ValueError("x and q must be 2-D of one shape, q int8")
+    if x.stride(1) != 1 or q.stride(1) != 1:
+        raise ValueError("rows must be contiguous")
+    _f32(scale, "scale")
+    _check(load().t2va_quantize_rows(int(x.shape[0]), int(x.shape[1]), _dtype_code(x.dtype), x.data_ptr(),
+                                     int(x.stride(0)), float(eps), q.data_ptr(), int(q.stride(0)),
+                                     scale.data_ptr(), _stream(stream)), "t2va_quantize_rows")
+
+
+def w8a8_linear(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,
+                y: torch.Tensor, bias: Optional[torch.Tensor] = None, stream=None):
+    """y = sx sw (xq . wq^T) + bias with an exact integer sum (t2va_w8a8_linear). xq [M, K]
+    and wq [N, K] int8, contiguous; y [M, N] bfloat16 or float32, contiguous."""
+    M, K = int(xq.shape[0]), int(xq.shape[1])
+    N = int(wq.shape[0])
+    if wq.shape[1] != K or tuple(y.shape) != (M, N):
+        raise ValueError("shapes do not match")
+    for t in (xq, wq, y):
+        if not t.is_contiguous():
+            raise ValueError("xq, wq and y must be contiguous")
+    if xq.dtype != torch.int8 or wq.dtype != torch.int8:
+        raise TypeError("xq and wq must be int8")
+    _f32(sx, "sx")
+    _f32(sw, "sw")
+    if bias is not None:
+        _f32(bias, "bias")
+    _check(load().t2va_w8a8_linear(M, N, K, xq.data_ptr(), sx.data_ptr(), wq.data_ptr(), sw.data_ptr(),
+                                   _opt(bias), _dtype_code(y.dtype), y.data_ptr(), _stream(stream)),
+           "t2va_w8a8_linear")
 
 
 def stage3_objective_noalloc(z_t, x0_teacher, x0_student, x0_student_tangent, t, zhat0,

@@ -281,6 +281,70 @@ size_t t2va_workspace_bytes(int batch, int num_modalities) {
   return ws_bytes(batch, num_modalities, dev.sm_count);
 }
 
+int t2va_quantize_rows(int64_t rows, int64_t cols, t2va_dtype dtype, const void* x, int64_t ld_x,
+                       float eps, int8_t* q, int64_t ld_q, float* scale, cudaStream_t stream) {
+  T2VA_TRY(check_dtype(dtype));
+  const int esz = dtype == T2VA_BFLOAT16 ? 2 : 4;
+  if (rows < 0 || cols < 0 || rows > INT32_MAX || ld_x < cols || ld_q < cols || !finite(eps) ||
+      !(eps > 0.f))
+    return T2VA_ERROR_INVALID_ARGUMENT;
+  if (rows == 0) return T2VA_SUCCESS;
+  if (x == nullptr || q == nullptr || scale == nullptr) return T2VA_ERROR_INVALID_ARGUMENT;
+  // every input row is whole 16-byte vectors starting on a 16-byte boundary; the codes
+  // of one vector (16 / element size bytes) are stored together, so output rows start
+  // on that boundary
+  if (cols % (16 / esz) != 0 || (ld_x * esz) % 16 != 0 || ld_q % (16 / esz) != 0)
+    return T2VA_ERROR_INVALID_ARGUMENT;
+  if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 4)) return T2VA_ERROR_MISALIGNED;
+  QuantArgs a;
+  a.rows = rows;
+  a.cols = cols;
+  a.x = x;
+  a.ld_x = ld_x;
+  a.q = q;
+  a.ld_q = ld_q;
+  a.scale = scale;
+  a.eps = eps;
+  if (launch_quantize_rows(a, dtype, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return T2VA_ERROR_CUDA;
+  }
+  return T2VA_SUCCESS;
+}
+
+int t2va_w8a8_linear(int64_t M, int64_t N, int64_t K, const int8_t* xq, const float* sx,
+                     const int8_t* wq, const float* sw, const float* bias, t2va_dtype out_dtype,
+                     void* y, cudaStream_t stream) {
+  T2VA_TRY(check_dtype(out_dtype));
+  if (M < 0 || N < 0 || K < 0) return T2VA_ERROR_INVALID_ARGUMENT;
+  if (M == 0 || N == 0) return T2VA_SUCCESS;
+  // the guarded shapes: M, N, K multiples of 128; K small enough that no INT32 sum of
+  // 127 x 127 products can overflow
+  if (M % 128 != 0 || N % 128 != 0 || K % 128 != 0 || K == 0 || K > kW8a8MaxK ||
+      M / gemm_tile_m() > 65535)
+    return T2VA_ERROR_INVALID_ARGUMENT;
+  if (xq == nullptr || sx == nullptr || wq == nullptr || sw == nullptr || y == nullptr)
+    return T2VA_ERROR_INVALID_ARGUMENT;
+  if (!aligned(xq, 16) || !aligned(wq, 16) || !aligned(sx, 4) || !aligned(sw, 4) ||
+      !aligned(bias, 8) || !aligned(y, 8))
+    return T2VA_ERROR_MISALIGNED;
+  GemmArgs a;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.xq = xq;
+  a.sx = sx;
+  a.wq = wq;
+  a.sw = sw;
+  a.bias = bias;
+  a.y = y;
+  if (launch_w8a8_gemm(a, out_dtype == T2VA_BFLOAT16, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return T2VA_ERROR_CUDA;
+  }
+  return T2VA_SUCCESS;
+}
+
 int t2va_workspace_init(void* workspace, size_t workspace_bytes, uint32_t timeout_ms,
                         cudaStream_t stream) {
   if (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < kWsHeaderBytes)

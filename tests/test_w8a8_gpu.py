@@ -1,0 +1,175 @@
+"""GPU parity of the post-scale W8A8 linear (t2va_quantize_rows, t2va_w8a8_linear)
+against the oracle in oracle/w8a8_oracle.py.
+
+Codes and scales are integers and float32 values decided in float32 on both sides, so
+they must match bit for bit. The integer sums are exact: with float32 output and unit
+scales y equals the sum exactly while |sum| < 2^24. The epilogue
+y = fma(float(acc), sx * sw, b) rounds float(acc) (once, only past 2^24), sx * sw and the
+fma, so |y - exact| <= 4 * 2^-24 (|sx sw acc| + |b|), plus one output ulp for bfloat16.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import joint_video_audio_02_b300 as t2va
+import oracle.w8a8_oracle as W8
+from joint_video_audio_02_b300.build import build
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build()
+    t2va.load()
+
+
+def _ulp_bf16(v):
+    _, e = np.frexp(np.abs(v))
+    return np.ldexp(1.0, np.maximum(e - 8, -133))
+
+
+def _rows(seed, M, K, dtype):
+    r = np.random.default_rng(seed)
+    x = (r.standard_normal((M, K)) * np.exp(r.uniform(-4, 4, (M, 1)))).astype(np.float32)
+    x[0, :] = 0.0                                   # an all-zero row: the eps scale
+    if M > 1:
+        x[1, :] = 0.0
+        x[1, : min(K, 8)] = np.array([127.0, 2.5, 3.5, -2.5, 0.5, -0.5, 1.5, 126.5], np.float32)[: min(K, 8)]
+    if M > 2:
+        x[2, :] *= 1e-9                             # below eps
+    t = torch.from_numpy(x)
+    if dtype == torch.bfloat16:
+        t = t.to(torch.bfloat16)
+    return t
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("M,K,pad", [(3, 8, 0), (5, 4096, 0), (7, 12352, 0), (6, 1024, 16), (130, 256, 8)])
+def test_quantize_rows_bit_exact(dtype, M, K, pad):
+    if dtype == torch.float32 and K % 4:
+        pytest.skip("float32 rows are whole 16-byte vectors")
+    x_host = _rows(M * 1000 + K, M, K, dtype)
+    xbuf = torch.zeros((M, K + pad), dtype=dtype, device="cuda")
+    xbuf[:, :K] = x_host.cuda()
+    x = xbuf[:, :K]
+    qbuf = torch.full((M, K + 16 * (pad > 0)), 99, dtype=torch.int8, device="cuda")
+    q = qbuf[:, :K]
+    s = torch.empty(M, device="cuda")
+    t2va.quantize_rows(x, q, s)
+    torch.cuda.synchronize()
+    ref_q, ref_s = W8.quantize_rows(x_host.float().numpy())
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), ref_q)
+    if pad:
+        assert torch.all(qbuf[:, K:] == 99)
+
+
+def test_quantize_codes_at_rounding_boundaries():
+    """Values at and within 3 ulps of (k + 1/2) s for random scales: the kernel forms the
+    quotient only near such boundaries, and its codes must still be those of the float32
+    quotient rounded half to even."""
+    r = np.random.default_rng(31)
+    M, K = 64, 1024
+    amax = r.uniform(0.1, 100.0, M).astype(np.float32)
+    s = (amax / np.float32(127)).astype(np.float32)
+    k = r.integers(-126, 126, (M, K)).astype(np.float32)
+    x = ((k + np.float32(0.5)) * s[:, None]).astype(np.float32)
+    xi = x.view(np.int32)
+    xi += r.integers(-3, 4, (M, K)).astype(np.int32)
+    x[:, 0] = amax                                   # the row maximum, so the scale is s
+    xd = torch.from_numpy(x).cuda()
+    q = torch.empty((M, K), dtype=torch.int8, device="cuda")
+    sc = torch.empty(M, device="cuda")
+    t2va.quantize_rows(xd, q, sc)
+    torch.cuda.synchronize()
+    ref_q, ref_s = W8.quantize_rows(x)
+    assert np.array_equal(sc.cpu().numpy(), ref_s)
+    assert np.array_equal(q.cpu().numpy(), ref_q)
+
+
+def _codes(seed, R, K, extreme=False):
+    r = np.random.default_rng(seed)
+    q = r.integers(-127, 128, (R, K)).astype(np.int8)
+    if extreme:
+        q[0, :] = 127
+        q[1, :] = -127
+    return q
+
+
+def _check_linear(y, acc, sx, sw, b, out_dtype):
+    exact = (sx.astype(np.float64)[:, None] * sw.astype(np.float64)[None, :]) * acc
+    mag = np.abs(exact)
+    if b is not None:
+        exact = exact + b.astype(np.float64)[None, :]
+        mag = mag + np.abs(b.astype(np.float64))[None, :]
+    bound = 4 * 2.0 ** -24 * mag + 1e-30
+    if out_dtype == torch.bfloat16:
+        bound = bound + _ulp_bf16(exact)
+    err = np.abs(y.astype(np.float64) - exact)
+    assert np.all(err <= bound), f"worst {np.max(err / bound):.2f} of bound"
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("M,N,K,bias", [(128, 128, 128, True), (256, 384, 512, False),
+                                        (384, 256, 4096, True), (128, 640, 1152, True)])
+def test_w8a8_linear_parity(out_dtype, M, N, K, bias):
+    xq = _codes(M + K, M, K, extreme=True)
+    wq = _codes(N + K + 1, N, K, extreme=True)
+    r = np.random.default_rng(K)
+    sx = r.uniform(1e-4, 0.05, M).astype(np.float32)
+    sw = r.uniform(1e-4, 0.05, N).astype(np.float32)
+    b = r.standard_normal(N).astype(np.float32) if bias else None
+    y = torch.empty((M, N), dtype=out_dtype, device="cuda")
+    t2va.w8a8_linear(torch.from_numpy(xq).cuda(), torch.from_numpy(sx).cuda(), torch.from_numpy(wq).cuda(),
+                     torch.from_numpy(sw).cuda(), y, None if b is None else torch.from_numpy(b).cuda())
+    torch.cuda.synchronize()
+    acc, _ = W8.w8a8_linear(xq, sx, wq, sw, b)
+    _check_linear(y.float().cpu().numpy(), acc, sx, sw, b, out_dtype)
+
+
+def test_w8a8_integer_sum_exact():
+    """Unit scales, no bias, float32 output: y is the integer sum itself (|sum| < 2^24 at
+    K = 1024), so every output must equal the oracle's sum exactly, tile edges included."""
+    M, N, K = 256, 256, 1024
+    xq, wq = _codes(11, M, K, extreme=True), _codes(12, N, K, extreme=True)
+    y = torch.empty((M, N), device="cuda")
+    one = lambda n: torch.ones(n, device="cuda")
+    t2va.w8a8_linear(torch.from_numpy(xq).cuda(), one(M), torch.from_numpy(wq).cuda(), one(N), y)
+    torch.cuda.synchronize()
+    acc = W8.int_dot(xq, wq)
+    assert np.abs(acc).max() < 2 ** 24
+    assert np.array_equal(y.cpu().numpy().astype(np.int64), acc)
+    assert int(acc[0, 0]) == K * 127 * 127 and int(acc[1, 0]) == -K * 127 * 127
+
+
+def test_w8a8_forward_matches_oracle():
+    """bf16 activations -> quantise -> linear against pre-quantised weights, the whole
+    operator, against the oracle's codes, scales and exact output."""
+    M, N, K = 256, 384, 2048
+    r = np.random.default_rng(21)
+    x = torch.from_numpy(r.standard_normal((M, K)).astype(np.float32)).to(torch.bfloat16)
+    w = r.standard_normal((N, K)).astype(np.float32) * 0.02
+    wq, sw = W8.quantize_rows(w)
+    b = r.standard_normal(N).astype(np.float32) * 0.1
+    xd = x.cuda()
+    q = torch.empty((M, K), dtype=torch.int8, device="cuda")
+    sx = torch.empty(M, device="cuda")
+    t2va.quantize_rows(xd, q, sx)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    t2va.w8a8_linear(q, sx, torch.from_numpy(wq).cuda(), torch.from_numpy(sw).cuda(), y,
+                     torch.from_numpy(b).cuda())
+    torch.cuda.synchronize()
+    ref_xq, ref_sx, acc, _ = W8.w8a8_forward(x.float().numpy(), wq, sw, b)
+    assert np.array_equal(q.cpu().numpy(), ref_xq)
+    assert np.array_equal(sx.cpu().numpy(), ref_sx)
+    _check_linear(y.float().cpu().numpy(), acc, ref_sx, sw, b, torch.bfloat16)
+
+
+def test_w8a8_guard():
+    z = torch.zeros((100, 128), dtype=torch.int8, device="cuda")
+    with pytest.raises(t2va.T2VAError) as e:
+        t2va.w8a8_linear(z, torch.ones(100, device="cuda"), torch.zeros((128, 128), dtype=torch.int8, device="cuda"),
+                         torch.ones(128, device="cuda"), torch.empty((100, 128), device="cuda"))
+    assert e.value.code == 1
