@@ -683,8 +683,12 @@ def run_reference(args, wl: S.Workload, world: int):
 
 # (M, N, K): M = video tokens of the 1024x1792 (28,672) and 512x768 (6,144) latents;
 # N = K = 4096, a projection width assumed for the 14B video backbone (not printed)
-W8A8_WORKLOADS = {"w8a8_28672x4096x4096_bf16": (28672, 4096, 4096),
-                  "w8a8_6144x4096x4096_bf16": (6144, 4096, 4096)}
+# the "tc" workloads store the codes as bfloat16 integers and contract them on the
+# tcgen05 tensor cores; the others use int8 codes and the warp-level INT8 MMA
+W8A8_WORKLOADS = {"w8a8_28672x4096x4096_bf16": (28672, 4096, 4096, "int8"),
+                  "w8a8_6144x4096x4096_bf16": (6144, 4096, 4096, "int8"),
+                  "w8a8tc_28672x4096x4096_bf16": (28672, 4096, 4096, "bf16"),
+                  "w8a8tc_6144x4096x4096_bf16": (6144, 4096, 4096, "bf16")}
 W8A8_METRIC = "W8A8 linear TOPS (per-row int8 quantisation + exact int8 GEMM, bf16 out)"
 
 
@@ -716,17 +720,19 @@ def run_w8a8(args, name: str):
 
     build()
     t2va.load()
-    M, N, K = W8A8_WORKLOADS[name]
+    M, N, K, codes = W8A8_WORKLOADS[name]
+    cdt = torch.bfloat16 if codes == "bf16" else torch.int8
     dev = torch.device("cuda", torch.cuda.current_device())
     props = torch.cuda.get_device_properties(dev)
     g = torch.Generator(device=dev).manual_seed(1234)
     x = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
     w = torch.randn((N, K), generator=g, device=dev) * 0.02
     bias = torch.randn(N, generator=g, device=dev) * 0.1
-    wq = torch.empty((N, K), dtype=torch.int8, device=dev)
+    wq = torch.empty((N, K), dtype=cdt, device=dev)
     sw = torch.empty(N, device=dev)
     t2va.quantize_rows(w, wq, sw)                     # static weight quantisation, once
-    xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+    xq = torch.empty((M, K), dtype=cdt, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
     sx = torch.empty(M, device=dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     st = torch.cuda.Stream(device=dev)
@@ -735,7 +741,7 @@ def run_w8a8(args, name: str):
         t2va.quantize_rows(x, xq, sx, stream=st)
 
     def linear():
-        t2va.w8a8_linear(xq, sx, wq, sw, y, bias, stream=st)
+        t2va.w8a8_linear(xq, sx, wq, sw, y, bias, status=status, stream=st)
 
     with torch.cuda.stream(st):
         quant()
@@ -783,8 +789,10 @@ def run_w8a8(args, name: str):
     time.sleep(0.02)
     sampler.stop()
     ms_q, ms_l = timed(g_q), timed(g_l)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during the benchmark")
     flops = 2.0 * M * N * K
-    q_bytes = M * K * 2 + M * K + 4 * M
+    q_bytes = M * K * 2 + M * K * (2 if codes == "bf16" else 1) + 4 * M
     peak_bf16 = None
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -817,16 +825,17 @@ def run_w8a8(args, name: str):
         "n_gpus": 1, "steps": reps * S_steps, "warmup": W, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
         "data": "synthetic",
-        "config": {"workload": name, "M": M, "N": N, "K": K, "x": "bf16 N(0,1)", "w": "N(0, 0.02^2), "
+        "config": {"workload": name, "M": M, "N": N, "K": K, "codes": codes, "x": "bf16 N(0,1)", "w": "N(0, 0.02^2), "
                    "quantised once per output channel", "out": "bf16", "bias": True,
                    "l2": "activations 235 MB / 50 MB and outputs larger than L2 at M = 28672 / 6144; "
                          "the 16.8 MB int8 weights stay in L2 by design",
                    "timing": "CUDA graphs of back-to-back steps, CUDA events on the launching stream"},
-        "roofline": {"kernel": "k_w8a8_gemm (mma.sync m16n8k32 s8)", "bound": "tensor",
+        "roofline": {"kernel": "k_w8a8_tc (tcgen05.mma kind::f16, TMA, TMEM)" if codes == "bf16"
+                               else "k_w8a8_gemm (mma.sync m16n8k32 s8)", "bound": "tensor",
                      "achieved": round(flops / (ms_l * 1e-3) / 1e12, 2), "peak": peak_bf16,
                      "unit": "TOPS", "frac": round(flops / (ms_l * 1e-3) / 1e12 / peak_bf16, 4),
-                     "peak_source": "measured dense bf16 TFLOP/s (MEASURED_PEAKS.json bf16_tflops): "
-                                    "sm_103a has no INT8 tcgen05.mma, so no INT8 peak is measured",
+                     "peak_source": "measured dense bf16 TFLOP/s (MEASURED_PEAKS.json bf16_tflops): the "
+                                    "tensor-core path runs bf16 MMAs; sm_103a has no INT8 tcgen05.mma",
                      "traffic": None, "mean_launch_us": round(ms_l * 1e3, 2)},
         "quantize_kernel": {"kernel": "k_quantize_rows", "achieved": round(q_bytes / (ms_q * 1e-3) / 1e9, 1),
                             "unit": "GB/s", "frac": round(q_bytes / (ms_q * 1e-3) / 1e9 / peak_hbm, 4),
@@ -863,7 +872,7 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.workload in W8A8_WORKLOADS:
         if args.impl == "reference":
-            M, N, K = W8A8_WORKLOADS[args.workload]
+            M, N, K, _ = W8A8_WORKLOADS[args.workload]
             base = w8a8_cpu_baseline(16, N, K, 10.0)
             print(json.dumps({"impl": "reference", "metric": W8A8_METRIC, "value": base["value"],
                               "unit": "TOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

@@ -59,7 +59,8 @@ extern "C" {
 
 typedef enum t2va_dtype {
   T2VA_FLOAT32 = 0,
-  T2VA_BFLOAT16 = 1
+  T2VA_BFLOAT16 = 1,
+  T2VA_INT8 = 2       /* W8A8 codes only */
 } t2va_dtype;
 
 /* Geometry of one modality: elements per sample and the distance (in elements)
@@ -81,9 +82,10 @@ enum {
 
 /* Device status bits, OR-ed into *status by the kernels. */
 #define T2VA_STATUS_BAD_TIMESTEP 0x1  /* a sample's t is outside (0, pi/2): its outputs are NaN    */
-/* Reserved (ABI version 1 kept them; no kernel of this library waits on another CTA or
- * checks the workspace, so neither is ever set). */
+/* A bounded pipeline wait of the tensor-core W8A8 kernel ran out (its output is
+ * incomplete). No objective kernel waits on another CTA, so the objective never sets it. */
 #define T2VA_STATUS_TIMEOUT 0x2
+/* Reserved (no kernel checks the workspace, so it is never set). */
 #define T2VA_STATUS_BAD_WORKSPACE 0x4
 
 /* Static description of a return code (never NULL). */
@@ -239,30 +241,39 @@ int t2va_stage3_objective_cfg(
  * --------------------------------------------------------------------------- */
 
 /* Quantise `rows` rows of `cols` elements (bfloat16 or float32, row i at
- * x + i * ld_x elements) into int8 codes (row i at q + i * ld_q bytes) and float32
- * scales scale[i] = max(amax_i, eps) / 127. Each code is rint(x / s) of the float32
- * quotient (IEEE division, ties to even), clipped to [-127, 127], so codes are exact
- * functions of the inputs. Use it for the activations before every linear and once
- * for each weight matrix (rows = output channels). Requires eps > 0, cols a multiple
- * of 16 bytes of input (8 bf16 or 4 float32 elements), ld_x * element size a
- * multiple of 16, ld_q a multiple of 16 / element size, x and q 16-byte aligned.
- * One warp per row: reads each input once (rows longer than 8 KiB are read a second
- * time, from L2) and writes 1 byte per element. One kernel on `stream`. */
+ * x + i * ld_x elements) into codes (row i at q + i * ld_q code elements) and float32
+ * scales scale[i] = max(amax_i, eps) / 127. Each code is rint of the correctly rounded
+ * float32 quotient x / s (ties to even), clipped to [-127, 127], so codes are exact
+ * functions of the inputs. `code_dtype` is T2VA_INT8 (one byte per code) or
+ * T2VA_BFLOAT16 (the same integers stored as bfloat16, exact, for the tensor-core
+ * contraction below). Use it for the activations before every linear and once for each
+ * weight matrix (rows = output channels). Requires eps > 0, cols a multiple of 16
+ * bytes of input (8 bf16 or 4 float32 elements), ld_x * element size a multiple of 16,
+ * ld_q a multiple of the codes written per input vector (16 / element size), x and q
+ * 16-byte aligned. One warp per row: reads each input once (rows longer than 8 KiB are
+ * read a second time, from L2). One kernel on `stream`. */
 int t2va_quantize_rows(int64_t rows, int64_t cols, t2va_dtype dtype, const void* x, int64_t ld_x,
-                       float eps, int8_t* q, int64_t ld_q, float* scale, cudaStream_t stream);
+                       float eps, t2va_dtype code_dtype, void* q, int64_t ld_q, float* scale,
+                       cudaStream_t stream);
 
 /* y[M][N] (row-major, bfloat16 or float32 per `out_dtype`) from activation codes
  * xq[M][K] with scales sx[M] and weight codes wq[N][K] with scales sw[N] (both
- * K-contiguous), and an optional bias[N] (NULL for none). The integer sum is exact;
- * the epilogue is y = fma(float(acc), sx_i * sw_j, b_j) in float32, rounded once to
- * `out_dtype`. Shapes are guarded as in the paper: M, N and K must be multiples of
- * 128 (else T2VA_ERROR_INVALID_ARGUMENT; the caller keeps its own BF16 linear for
- * other shapes), and K <= 131072 so that no INT32 sum can overflow. sm_103a has no
- * INT8 form of the fifth-generation tensor-core MMA, so the contraction runs on the
- * warp-level INT8 MMA. One kernel on `stream`. */
-int t2va_w8a8_linear(int64_t M, int64_t N, int64_t K, const int8_t* xq, const float* sx,
-                     const int8_t* wq, const float* sw, const float* bias, t2va_dtype out_dtype,
-                     void* y, cudaStream_t stream);
+ * K-contiguous, of `code_dtype`), and an optional bias[N] (NULL for none). The integer
+ * sum is exact; the epilogue is y = fma(float(acc), sx_i * sw_j, b_j) in float32,
+ * rounded once to `out_dtype`. Shapes are guarded as in the paper: M, N and K must be
+ * multiples of 128 (else T2VA_ERROR_INVALID_ARGUMENT; the caller keeps its own BF16
+ * linear for other shapes), and K <= 131072 so that no INT32 sum can overflow.
+ *   - T2VA_INT8 codes: the warp-level INT8 MMA (mma.sync m16n8k32 s8). sm_103a has no
+ *     INT8 form of the fifth-generation tensor-core MMA.
+ *   - T2VA_BFLOAT16 codes: tcgen05.mma (bf16 x bf16 -> f32 in TMEM), K summed in chunks
+ *     of 1024 whose float32 sums stay below 2^24 and are therefore exact integers, the
+ *     chunks added as int32. Same result, at the bf16 tensor-core rate. Needs y 16-byte
+ *     aligned. Its pipeline waits are bounded: a wait that runs out sets
+ *     T2VA_STATUS_TIMEOUT in `status` (may be NULL) and leaves y incomplete.
+ * One kernel on `stream`. */
+int t2va_w8a8_linear(int64_t M, int64_t N, int64_t K, t2va_dtype code_dtype, const void* xq,
+                     const float* sx, const void* wq, const float* sw, const float* bias,
+                     t2va_dtype out_dtype, void* y, int* status, cudaStream_t stream);
 
 /* Bytes of the library's own scratch array used by
  * t2va_stage3_objective_noalloc (1 MiB). Every GPU that loads the library holds

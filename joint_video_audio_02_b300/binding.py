@@ -25,6 +25,7 @@ c_int, c_float, c_void_p, c_size_t, c_int64, c_uint32 = (
 
 T2VA_FLOAT32 = 0
 T2VA_BFLOAT16 = 1
+T2VA_INT8 = 2
 MAX_MODALITIES = 4
 
 STATUS_BAD_TIMESTEP = 0x1
@@ -86,9 +87,9 @@ def _declare(lib):
                                               c_float, c_float, c_float, c_float, P, c_float, c_float,
                                               P, P, c_int, P, P, P, P, P, P, c_size_t, P, P]
     lib.t2va_stage3_objective_cfg.restype = c_int
-    lib.t2va_quantize_rows.argtypes = [c_int64, c_int64, c_int, P, c_int64, c_float, P, c_int64, P, P]
+    lib.t2va_quantize_rows.argtypes = [c_int64, c_int64, c_int, P, c_int64, c_float, c_int, P, c_int64, P, P]
     lib.t2va_quantize_rows.restype = c_int
-    lib.t2va_w8a8_linear.argtypes = [c_int64, c_int64, c_int64, P, P, P, P, P, c_int, P, P]
+    lib.t2va_w8a8_linear.argtypes = [c_int64, c_int64, c_int64, c_int, P, P, P, P, P, c_int, P, P, P]
     lib.t2va_w8a8_linear.restype = c_int
 
 
@@ -301,24 +302,35 @@ def stage3_objective_cfg(z_t, x0_teacher, x0_student, x0_student_tangent, t, zha
 W8A8_EPS = 1e-4
 
 
+def _code_dtype(dt: torch.dtype) -> int:
+    if dt == torch.int8:
+        return T2VA_INT8
+    if dt == torch.bfloat16:
+        return T2VA_BFLOAT16
+    raise TypeError("codes are int8, or bfloat16 for the tensor-core contraction")
+
+
 def quantize_rows(x: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, eps: float = W8A8_EPS,
                   stream=None):
-    """Per-row dynamic int8 quantisation of a 2-D CUDA tensor (t2va_quantize_rows): codes
-    into `q` (int8, same shape, rows 16-byte aligned) and scales into `scale` (float32)."""
-    if x.dim() != 2 or q.dim() != 2 or q.shape != x.shape or q.dtype != torch.int8:
-        raise ValueError("x and q must be 2-D of one shape, q int8")
+    """Per-row dynamic quantisation of a 2-D CUDA tensor (t2va_quantize_rows): codes into
+    `q` (int8, or bfloat16 holding the same integers; same shape, rows 16-byte aligned)
+    and scales into `scale` (float32)."""
+    if x.dim() != 2 or q.dim() != 2 or q.shape != x.shape:
+        raise ValueError("x and q must be 2-D of one shape")
     if x.stride(1) != 1 or q.stride(1) != 1:
         raise ValueError("rows must be contiguous")
     _f32(scale, "scale")
     _check(load().t2va_quantize_rows(int(x.shape[0]), int(x.shape[1]), _dtype_code(x.dtype), x.data_ptr(),
-                                     int(x.stride(0)), float(eps), q.data_ptr(), int(q.stride(0)),
-                                     scale.data_ptr(), _stream(stream)), "t2va_quantize_rows")
+                                     int(x.stride(0)), float(eps), _code_dtype(q.dtype), q.data_ptr(),
+                                     int(q.stride(0)), scale.data_ptr(), _stream(stream)), "t2va_quantize_rows")
 
 
 def w8a8_linear(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,
-                y: torch.Tensor, bias: Optional[torch.Tensor] = None, stream=None):
+                y: torch.Tensor, bias: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                stream=None):
     """y = sx sw (xq . wq^T) + bias with an exact integer sum (t2va_w8a8_linear). xq [M, K]
-    and wq [N, K] int8, contiguous; y [M, N] bfloat16 or float32, contiguous."""
+    and wq [N, K] are codes (int8: warp-level INT8 MMA; bfloat16 integers: tcgen05 tensor
+    cores), contiguous; y [M, N] bfloat16 or float32, contiguous."""
     M, K = int(xq.shape[0]), int(xq.shape[1])
     N = int(wq.shape[0])
     if wq.shape[1] != K or tuple(y.shape) != (M, N):
@@ -326,15 +338,15 @@ def w8a8_linear(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.
     for t in (xq, wq, y):
         if not t.is_contiguous():
             raise ValueError("xq, wq and y must be contiguous")
-    if xq.dtype != torch.int8 or wq.dtype != torch.int8:
-        raise TypeError("xq and wq must be int8")
+    if xq.dtype != wq.dtype:
+        raise TypeError("xq and wq must have one code dtype")
     _f32(sx, "sx")
     _f32(sw, "sw")
     if bias is not None:
         _f32(bias, "bias")
-    _check(load().t2va_w8a8_linear(M, N, K, xq.data_ptr(), sx.data_ptr(), wq.data_ptr(), sw.data_ptr(),
-                                   _opt(bias), _dtype_code(y.dtype), y.data_ptr(), _stream(stream)),
-           "t2va_w8a8_linear")
+    _check(load().t2va_w8a8_linear(M, N, K, _code_dtype(xq.dtype), xq.data_ptr(), sx.data_ptr(), wq.data_ptr(),
+                                   sw.data_ptr(), _opt(bias), _dtype_code(y.dtype), y.data_ptr(), _opt(status),
+                                   _stream(stream)), "t2va_w8a8_linear")
 
 
 def stage3_objective_noalloc(z_t, x0_teacher, x0_student, x0_student_tangent, t, zhat0,

@@ -282,8 +282,10 @@ size_t t2va_workspace_bytes(int batch, int num_modalities) {
 }
 
 int t2va_quantize_rows(int64_t rows, int64_t cols, t2va_dtype dtype, const void* x, int64_t ld_x,
-                       float eps, int8_t* q, int64_t ld_q, float* scale, cudaStream_t stream) {
+                       float eps, t2va_dtype code_dtype, void* q, int64_t ld_q, float* scale,
+                       cudaStream_t stream) {
   T2VA_TRY(check_dtype(dtype));
+  if (code_dtype != T2VA_INT8 && code_dtype != T2VA_BFLOAT16) return T2VA_ERROR_UNSUPPORTED_DTYPE;
   const int esz = dtype == T2VA_BFLOAT16 ? 2 : 4;
   if (rows < 0 || cols < 0 || rows > INT32_MAX || ld_x < cols || ld_q < cols || !finite(eps) ||
       !(eps > 0.f))
@@ -291,7 +293,7 @@ int t2va_quantize_rows(int64_t rows, int64_t cols, t2va_dtype dtype, const void*
   if (rows == 0) return T2VA_SUCCESS;
   if (x == nullptr || q == nullptr || scale == nullptr) return T2VA_ERROR_INVALID_ARGUMENT;
   // every input row is whole 16-byte vectors starting on a 16-byte boundary; the codes
-  // of one vector (16 / element size bytes) are stored together, so output rows start
+  // of one vector (16 / element size of them) are stored together, so output rows start
   // on that boundary
   if (cols % (16 / esz) != 0 || (ld_x * esz) % 16 != 0 || ld_q % (16 / esz) != 0)
     return T2VA_ERROR_INVALID_ARGUMENT;
@@ -299,6 +301,7 @@ int t2va_quantize_rows(int64_t rows, int64_t cols, t2va_dtype dtype, const void*
   QuantArgs a;
   a.rows = rows;
   a.cols = cols;
+  a.codes_bf16 = code_dtype == T2VA_BFLOAT16;
   a.x = x;
   a.ld_x = ld_x;
   a.q = q;
@@ -312,10 +315,11 @@ int t2va_quantize_rows(int64_t rows, int64_t cols, t2va_dtype dtype, const void*
   return T2VA_SUCCESS;
 }
 
-int t2va_w8a8_linear(int64_t M, int64_t N, int64_t K, const int8_t* xq, const float* sx,
-                     const int8_t* wq, const float* sw, const float* bias, t2va_dtype out_dtype,
-                     void* y, cudaStream_t stream) {
+int t2va_w8a8_linear(int64_t M, int64_t N, int64_t K, t2va_dtype code_dtype, const void* xq,
+                     const float* sx, const void* wq, const float* sw, const float* bias,
+                     t2va_dtype out_dtype, void* y, int* status, cudaStream_t stream) {
   T2VA_TRY(check_dtype(out_dtype));
+  if (code_dtype != T2VA_INT8 && code_dtype != T2VA_BFLOAT16) return T2VA_ERROR_UNSUPPORTED_DTYPE;
   if (M < 0 || N < 0 || K < 0) return T2VA_ERROR_INVALID_ARGUMENT;
   if (M == 0 || N == 0) return T2VA_SUCCESS;
   // the guarded shapes: M, N, K multiples of 128; K small enough that no INT32 sum of
@@ -325,20 +329,24 @@ int t2va_w8a8_linear(int64_t M, int64_t N, int64_t K, const int8_t* xq, const fl
     return T2VA_ERROR_INVALID_ARGUMENT;
   if (xq == nullptr || sx == nullptr || wq == nullptr || sw == nullptr || y == nullptr)
     return T2VA_ERROR_INVALID_ARGUMENT;
+  const bool tc = code_dtype == T2VA_BFLOAT16;
   if (!aligned(xq, 16) || !aligned(wq, 16) || !aligned(sx, 4) || !aligned(sw, 4) ||
-      !aligned(bias, 8) || !aligned(y, 8))
+      !aligned(bias, 4) || !aligned(y, tc ? 16 : 8) || !aligned(status, 4))
     return T2VA_ERROR_MISALIGNED;
   GemmArgs a;
   a.M = M;
   a.N = N;
   a.K = K;
-  a.xq = xq;
+  a.xq = reinterpret_cast<const int8_t*>(xq);
   a.sx = sx;
-  a.wq = wq;
+  a.wq = reinterpret_cast<const int8_t*>(wq);
   a.sw = sw;
   a.bias = bias;
   a.y = y;
-  if (launch_w8a8_gemm(a, out_dtype == T2VA_BFLOAT16, stream) != cudaSuccess) {
+  a.status = status;
+  const cudaError_t e = tc ? launch_w8a8_tc(a, out_dtype == T2VA_BFLOAT16, stream)
+                           : launch_w8a8_gemm(a, out_dtype == T2VA_BFLOAT16, stream);
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return T2VA_ERROR_CUDA;
   }

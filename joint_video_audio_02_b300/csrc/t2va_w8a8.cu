@@ -68,27 +68,57 @@ __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
          ((uint32_t)(d & 0xff) << 24);
 }
 
-// Codes of one 16-byte input vector, stored at q (8 codes for bf16, 4 for float32).
-__device__ __forceinline__ void store_codes(const uint4& r, float s, float inv, int8_t* q,
-                                            __nv_bfloat16) {
+__device__ __forceinline__ uint32_t pack_bf16(int a, int b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn((float)a, (float)b);  // exact: |a|, |b| <= 127
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// The codes of one 16-byte input vector (8 for bf16 input, 4 for float32).
+template <typename T>
+__device__ __forceinline__ void codes_of(const uint4& r, float s, float inv, int (&c)[16 / sizeof(T)]);
+
+template <>
+__device__ __forceinline__ void codes_of<__nv_bfloat16>(const uint4& r, float s, float inv, int (&c)[8]) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
-  int c[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float2 f = __bfloat1622float2(h[i]);
     c[2 * i] = code_of(f.x, s, inv);
     c[2 * i + 1] = code_of(f.y, s, inv);
   }
-  *reinterpret_cast<uint2*>(q) = make_uint2(pack4(c[0], c[1], c[2], c[3]), pack4(c[4], c[5], c[6], c[7]));
 }
 
-__device__ __forceinline__ void store_codes(const uint4& r, float s, float inv, int8_t* q, float) {
+template <>
+__device__ __forceinline__ void codes_of<float>(const uint4& r, float s, float inv, int (&c)[4]) {
   const float* f = reinterpret_cast<const float*>(&r);
-  *reinterpret_cast<uint32_t*>(q) = pack4(code_of(f[0], s, inv), code_of(f[1], s, inv),
-                                          code_of(f[2], s, inv), code_of(f[3], s, inv));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = code_of(f[i], s, inv);
 }
 
-template <typename T>
+// Store the codes of input vector v of a row: int8 (8 or 4 bytes) or bfloat16 integers
+// (16 or 8 bytes).
+template <typename T, bool BF16_CODES>
+__device__ __forceinline__ void store_codes(const uint4& r, float s, float inv, void* q, int64_t v) {
+  constexpr int VE = 16 / sizeof(T);
+  int c[VE];
+  codes_of<T>(r, s, inv, c);
+  if constexpr (BF16_CODES) {
+    __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(q) + v * VE;
+    if constexpr (VE == 8)
+      *reinterpret_cast<uint4*>(d) = make_uint4(pack_bf16(c[0], c[1]), pack_bf16(c[2], c[3]),
+                                                pack_bf16(c[4], c[5]), pack_bf16(c[6], c[7]));
+    else
+      *reinterpret_cast<uint2*>(d) = make_uint2(pack_bf16(c[0], c[1]), pack_bf16(c[2], c[3]));
+  } else {
+    int8_t* d = reinterpret_cast<int8_t*>(q) + v * VE;
+    if constexpr (VE == 8)
+      *reinterpret_cast<uint2*>(d) = make_uint2(pack4(c[0], c[1], c[2], c[3]), pack4(c[4], c[5], c[6], c[7]));
+    else
+      *reinterpret_cast<uint32_t*>(d) = pack4(c[0], c[1], c[2], c[3]);
+  }
+}
+
+template <typename T, bool BF16_CODES>
 __global__ void __launch_bounds__(kQThreads) k_quantize_rows(const __grid_constant__ QuantArgs a) {
   constexpr int VE = 16 / sizeof(T);
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -115,14 +145,15 @@ __global__ void __launch_bounds__(kQThreads) k_quantize_rows(const __grid_consta
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   const float s = __fdiv_rn(fmaxf(m, a.eps), 127.f);
   const float inv = __frcp_rn(s);
-  int8_t* q = a.q + row * a.ld_q;
+  void* q = BF16_CODES ? (void*)(reinterpret_cast<__nv_bfloat16*>(a.q) + row * a.ld_q)
+                       : (void*)(reinterpret_cast<int8_t*>(a.q) + row * a.ld_q);
 #pragma unroll
   for (int c = 0; c < kQCache; ++c) {
     const int64_t v = (int64_t)c * 32 + lane;
-    if (v < nvec) store_codes(cache[c], s, inv, q + v * VE, T());
+    if (v < nvec) store_codes<T, BF16_CODES>(cache[c], s, inv, q, v);
   }
   for (int64_t v = (int64_t)kQCache * 32 + lane; v < nvec; v += 32)
-    store_codes(*reinterpret_cast<const uint4*>(x + v * VE), s, inv, q + v * VE, T());
+    store_codes<T, BF16_CODES>(*reinterpret_cast<const uint4*>(x + v * VE), s, inv, q, v);
   if (lane == 0) a.scale[row] = s;
 }
 
@@ -280,11 +311,12 @@ cudaError_t launch_pdl_args(K kern, dim3 grid, int threads, size_t smem, cudaStr
 }  // namespace
 
 cudaError_t launch_quantize_rows(const QuantArgs& a, t2va_dtype dt, cudaStream_t st) {
+  const dim3 grid((unsigned)((a.rows + kQRows - 1) / kQRows));
   if (dt == T2VA_BFLOAT16)
-    return launch_pdl_args(k_quantize_rows<__nv_bfloat16>, dim3((unsigned)((a.rows + kQRows - 1) / kQRows)),
-                           kQThreads, 0, st, a);
-  return launch_pdl_args(k_quantize_rows<float>, dim3((unsigned)((a.rows + kQRows - 1) / kQRows)),
-                         kQThreads, 0, st, a);
+    return a.codes_bf16 ? launch_pdl_args(k_quantize_rows<__nv_bfloat16, true>, grid, kQThreads, 0, st, a)
+                        : launch_pdl_args(k_quantize_rows<__nv_bfloat16, false>, grid, kQThreads, 0, st, a);
+  return a.codes_bf16 ? launch_pdl_args(k_quantize_rows<float, true>, grid, kQThreads, 0, st, a)
+                      : launch_pdl_args(k_quantize_rows<float, false>, grid, kQThreads, 0, st, a);
 }
 
 int gemm_tile_m() { return kBM; }

@@ -100,16 +100,21 @@ def test_host_validation_without_device(lib):
     assert lib.t2va_stage3_objective_cfg(*cfg(_p(ok + 8, ok), g_ok)) == 3
     # W8A8: the paper's shape guard and the alignment rules are host checks
     a16 = 0x20000
-    assert lib.t2va_quantize_rows(4, 100, 1, a16, 100, 1e-4, a16, 112, a16, None) == 1   # cols % 8
-    assert lib.t2va_quantize_rows(4, 128, 1, a16, 128, 0.0, a16, 128, a16, None) == 1    # eps <= 0
-    assert lib.t2va_quantize_rows(4, 128, 1, a16, 120, 1e-4, a16, 128, a16, None) == 1   # ld_x < cols
-    assert lib.t2va_quantize_rows(4, 128, 1, a16 + 8, 128, 1e-4, a16, 128, a16, None) == 3
-    assert lib.t2va_quantize_rows(0, 128, 1, None, 128, 1e-4, None, 128, None, None) == 0
+    I8, BF = 2, 1
+    assert lib.t2va_quantize_rows(4, 100, 1, a16, 100, 1e-4, I8, a16, 112, a16, None) == 1   # cols % 8
+    assert lib.t2va_quantize_rows(4, 128, 1, a16, 128, 0.0, I8, a16, 128, a16, None) == 1    # eps <= 0
+    assert lib.t2va_quantize_rows(4, 128, 1, a16, 120, 1e-4, I8, a16, 128, a16, None) == 1   # ld_x < cols
+    assert lib.t2va_quantize_rows(4, 128, 1, a16 + 8, 128, 1e-4, I8, a16, 128, a16, None) == 3
+    assert lib.t2va_quantize_rows(4, 128, 1, a16, 128, 1e-4, 0, a16, 128, a16, None) == 2    # float32 codes
+    assert lib.t2va_quantize_rows(0, 128, 1, None, 128, 1e-4, BF, None, 128, None, None) == 0
     for M, N, K in ((100, 128, 128), (128, 96, 128), (128, 128, 192), (128, 128, 0), (128, 128, 131200)):
-        assert lib.t2va_w8a8_linear(M, N, K, a16, a16, a16, a16, None, 0, a16, None) == 1
-    assert lib.t2va_w8a8_linear(128, 128, 128, a16 + 4, a16, a16, a16, None, 0, a16, None) == 3
-    assert lib.t2va_w8a8_linear(128, 128, 128, a16, a16, a16, a16, None, 7, a16, None) == 2
-    assert lib.t2va_w8a8_linear(0, 128, 128, None, None, None, None, None, 0, None, None) == 0
+        for code in (I8, BF):
+            assert lib.t2va_w8a8_linear(M, N, K, code, a16, a16, a16, a16, None, 0, a16, None, None) == 1
+    assert lib.t2va_w8a8_linear(128, 128, 128, I8, a16 + 4, a16, a16, a16, None, 0, a16, None, None) == 3
+    assert lib.t2va_w8a8_linear(128, 128, 128, BF, a16, a16, a16, a16, None, 0, a16 + 8, None, None) == 3
+    assert lib.t2va_w8a8_linear(128, 128, 128, I8, a16, a16, a16, a16, None, 7, a16, None, None) == 2
+    assert lib.t2va_w8a8_linear(128, 128, 128, 0, a16, a16, a16, a16, None, 0, a16, None, None) == 2
+    assert lib.t2va_w8a8_linear(0, 128, 128, I8, None, None, None, None, None, 0, None, None, None) == 0
     # workspace checks come after the argument checks and need no device either
     assert lib.t2va_workspace_init(None, 1024, 0, None) == 4
     assert lib.t2va_workspace_init(ok + 4, 1024, 0, None) == 4

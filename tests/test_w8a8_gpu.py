@@ -1,5 +1,7 @@
 """GPU parity of the post-scale W8A8 linear (t2va_quantize_rows, t2va_w8a8_linear)
-against the oracle in oracle/w8a8_oracle.py.
+against the oracle in oracle/w8a8_oracle.py, for both contractions: int8 codes on the
+warp-level INT8 MMA, and the same codes stored as bfloat16 integers on the tcgen05
+tensor cores (float32 sums over K chunks of 1024, below 2^24, added as int32).
 
 Codes and scales are integers and float32 values decided in float32 on both sides, so
 they must match bit for bit. The integer sums are exact: with float32 output and unit
@@ -45,23 +47,28 @@ def _rows(seed, M, K, dtype):
     return t
 
 
+CODES = [torch.int8, torch.bfloat16]
+
+
+@pytest.mark.parametrize("code", CODES, ids=["int8", "bf16codes"])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("M,K,pad", [(3, 8, 0), (5, 4096, 0), (7, 12352, 0), (6, 1024, 16), (130, 256, 8)])
-def test_quantize_rows_bit_exact(dtype, M, K, pad):
+def test_quantize_rows_bit_exact(code, dtype, M, K, pad):
     if dtype == torch.float32 and K % 4:
         pytest.skip("float32 rows are whole 16-byte vectors")
     x_host = _rows(M * 1000 + K, M, K, dtype)
     xbuf = torch.zeros((M, K + pad), dtype=dtype, device="cuda")
     xbuf[:, :K] = x_host.cuda()
     x = xbuf[:, :K]
-    qbuf = torch.full((M, K + 16 * (pad > 0)), 99, dtype=torch.int8, device="cuda")
+    qbuf = torch.full((M, K + 16 * (pad > 0)), 99, dtype=code, device="cuda")
     q = qbuf[:, :K]
     s = torch.empty(M, device="cuda")
     t2va.quantize_rows(x, q, s)
     torch.cuda.synchronize()
     ref_q, ref_s = W8.quantize_rows(x_host.float().numpy())
     assert np.array_equal(s.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
-    assert np.array_equal(q.cpu().numpy(), ref_q)
+    got = q.cpu().float().numpy() if code == torch.bfloat16 else q.cpu().numpy()
+    assert np.array_equal(got, ref_q.astype(got.dtype))
     if pad:
         assert torch.all(qbuf[:, K:] == 99)
 
@@ -111,10 +118,17 @@ def _check_linear(y, acc, sx, sw, b, out_dtype):
     assert np.all(err <= bound), f"worst {np.max(err / bound):.2f} of bound"
 
 
+def _dev_codes(q, code):
+    t = torch.from_numpy(q).cuda()
+    return t.to(torch.bfloat16) if code == torch.bfloat16 else t
+
+
+@pytest.mark.parametrize("code", CODES, ids=["int8", "bf16codes"])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("M,N,K,bias", [(128, 128, 128, True), (256, 384, 512, False),
-                                        (384, 256, 4096, True), (128, 640, 1152, True)])
-def test_w8a8_linear_parity(out_dtype, M, N, K, bias):
+                                        (384, 256, 4096, True), (128, 640, 1152, True),
+                                        (256, 128, 8192, False)])
+def test_w8a8_linear_parity(code, out_dtype, M, N, K, bias):
     xq = _codes(M + K, M, K, extreme=True)
     wq = _codes(N + K + 1, N, K, extreme=True)
     r = np.random.default_rng(K)
@@ -122,29 +136,46 @@ def test_w8a8_linear_parity(out_dtype, M, N, K, bias):
     sw = r.uniform(1e-4, 0.05, N).astype(np.float32)
     b = r.standard_normal(N).astype(np.float32) if bias else None
     y = torch.empty((M, N), dtype=out_dtype, device="cuda")
-    t2va.w8a8_linear(torch.from_numpy(xq).cuda(), torch.from_numpy(sx).cuda(), torch.from_numpy(wq).cuda(),
-                     torch.from_numpy(sw).cuda(), y, None if b is None else torch.from_numpy(b).cuda())
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t2va.w8a8_linear(_dev_codes(xq, code), torch.from_numpy(sx).cuda(), _dev_codes(wq, code),
+                     torch.from_numpy(sw).cuda(), y, None if b is None else torch.from_numpy(b).cuda(),
+                     status=st)
     torch.cuda.synchronize()
+    assert st.item() == 0
     acc, _ = W8.w8a8_linear(xq, sx, wq, sw, b)
     _check_linear(y.float().cpu().numpy(), acc, sx, sw, b, out_dtype)
 
 
-def test_w8a8_integer_sum_exact():
-    """Unit scales, no bias, float32 output: y is the integer sum itself (|sum| < 2^24 at
-    K = 1024), so every output must equal the oracle's sum exactly, tile edges included."""
-    M, N, K = 256, 256, 1024
-    xq, wq = _codes(11, M, K, extreme=True), _codes(12, N, K, extreme=True)
-    y = torch.empty((M, N), device="cuda")
+@pytest.mark.parametrize("code", CODES, ids=["int8", "bf16codes"])
+def test_w8a8_integer_sum_exact(code):
+    """Unit scales, no bias, float32 output: y is the integer sum itself while |sum| < 2^24,
+    so every output must equal the oracle's sum exactly, tile edges included. K = 1024
+    holds one full chunk of the tensor-core path at its largest possible magnitude,
+    1024 x 127 x 127 = 16,516,096 (just below 2^24); K = 3072 adds chunks of opposite
+    sign that must cancel exactly."""
     one = lambda n: torch.ones(n, device="cuda")
-    t2va.w8a8_linear(torch.from_numpy(xq).cuda(), one(M), torch.from_numpy(wq).cuda(), one(N), y)
-    torch.cuda.synchronize()
-    acc = W8.int_dot(xq, wq)
-    assert np.abs(acc).max() < 2 ** 24
-    assert np.array_equal(y.cpu().numpy().astype(np.int64), acc)
-    assert int(acc[0, 0]) == K * 127 * 127 and int(acc[1, 0]) == -K * 127 * 127
+    for K in (1024, 3072):
+        M, N = 256, 256
+        xq, wq = _codes(11 + K, M, K, extreme=True), _codes(12 + K, N, K, extreme=True)
+        if K == 3072:
+            wq[2, :1024], wq[2, 1024:2048], wq[2, 2048:] = 127, -127, 0   # +16.5M, -16.5M, 0
+            xq[0, :] = 127
+        y = torch.empty((M, N), device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        t2va.w8a8_linear(_dev_codes(xq, code), one(M), _dev_codes(wq, code), one(N), y, status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        acc = W8.int_dot(xq, wq)
+        ok = np.abs(acc) < 2 ** 24
+        assert np.array_equal(y.cpu().numpy().astype(np.int64)[ok], acc[ok])
+        if K == 1024:
+            assert int(acc[0, 0]) == K * 127 * 127 and int(acc[1, 0]) == -K * 127 * 127
+        else:
+            assert int(acc[0, 2]) == 0 and float(y[0, 2]) == 0.0
 
 
-def test_w8a8_forward_matches_oracle():
+@pytest.mark.parametrize("code", CODES, ids=["int8", "bf16codes"])
+def test_w8a8_forward_matches_oracle(code):
     """bf16 activations -> quantise -> linear against pre-quantised weights, the whole
     operator, against the oracle's codes, scales and exact output."""
     M, N, K = 256, 384, 2048
@@ -154,15 +185,15 @@ def test_w8a8_forward_matches_oracle():
     wq, sw = W8.quantize_rows(w)
     b = r.standard_normal(N).astype(np.float32) * 0.1
     xd = x.cuda()
-    q = torch.empty((M, K), dtype=torch.int8, device="cuda")
+    q = torch.empty((M, K), dtype=code, device="cuda")
     sx = torch.empty(M, device="cuda")
     t2va.quantize_rows(xd, q, sx)
     y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    t2va.w8a8_linear(q, sx, torch.from_numpy(wq).cuda(), torch.from_numpy(sw).cuda(), y,
+    t2va.w8a8_linear(q, sx, _dev_codes(wq, code), torch.from_numpy(sw).cuda(), y,
                      torch.from_numpy(b).cuda())
     torch.cuda.synchronize()
     ref_xq, ref_sx, acc, _ = W8.w8a8_forward(x.float().numpy(), wq, sw, b)
-    assert np.array_equal(q.cpu().numpy(), ref_xq)
+    assert np.array_equal(q.cpu().float().numpy().astype(np.int64), ref_xq.astype(np.int64))
     assert np.array_equal(sx.cpu().numpy(), ref_sx)
     _check_linear(y.float().cpu().numpy(), acc, ref_sx, sw, b, torch.bfloat16)
 
