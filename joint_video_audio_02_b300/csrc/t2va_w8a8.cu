@@ -7,9 +7,10 @@
 // with the integer products summed exactly in INT32 over the whole K and both scales
 // applied once, in the epilogue.
 //
-// k_quantize_rows: one warp per row, eight rows per CTA. The row is read once into
-// registers (16 vectors per lane: 4096 bf16 elements; longer rows read the rest again,
-// from L2), its absolute maximum is reduced by shuffles, and every code is rint of the
+// k_quantize_rows: kTPR threads per row. The row is read once into registers (512
+// vectors per row: 4096 bf16 elements; longer rows read the rest again, from L2), its
+// absolute maximum is reduced by shuffles (and shared memory across the row's warps),
+// and every code is rint of the
 // correctly rounded float32 quotient x / s (ties to even), so the codes are bit-exact
 // functions of the inputs; the quotient is formed only near a rounding boundary (see
 // code_of).
@@ -30,8 +31,9 @@ namespace {
 // ---------------------------------------------------------------------------
 
 constexpr int kQThreads = 256;
-constexpr int kQRows = kQThreads / 32;  // one warp per row
-constexpr int kQCache = 16;             // 16-byte vectors per lane kept in registers
+constexpr int kTPR = 32;                    // threads per row
+constexpr int kQRows = kQThreads / kTPR;    // rows per CTA
+constexpr int kQCache = 512 / kTPR;         // 16-byte vectors per thread kept in registers
 
 __device__ __forceinline__ float amax_of(const uint4& r, __nv_bfloat16) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
@@ -121,40 +123,51 @@ __device__ __forceinline__ void store_codes(const uint4& r, float s, float inv, 
 template <typename T, bool BF16_CODES>
 __global__ void __launch_bounds__(kQThreads) k_quantize_rows(const __grid_constant__ QuantArgs a) {
   constexpr int VE = 16 / sizeof(T);
+  constexpr int kWarpsPerRow = kTPR >= 32 ? kTPR / 32 : 1;
+  __shared__ float red[kQThreads / 32];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * kQRows + (threadIdx.x >> 5);
-  if (row >= a.rows) return;  // whole warps only: the shuffles below stay warp-uniform
-  const T* x = reinterpret_cast<const T*>(a.x) + row * a.ld_x;
-  const int64_t nvec = a.cols / VE;
+  const int t = threadIdx.x % kTPR;
+  const int64_t row = (int64_t)blockIdx.x * kQRows + threadIdx.x / kTPR;
+  const bool live = row < a.rows;
+  const T* x = reinterpret_cast<const T*>(a.x) + (live ? row : 0) * a.ld_x;
+  const int64_t nvec = live ? a.cols / VE : 0;
   uint4 cache[kQCache];
   float m = 0.f;
 #pragma unroll
   for (int c = 0; c < kQCache; ++c) {
-    const int64_t v = (int64_t)c * 32 + lane;
+    const int64_t v = (int64_t)c * kTPR + t;
     if (v < nvec) {
       cache[c] = ld_stream16(x + v * VE);
       m = fmaxf(m, amax_of(cache[c], T()));
     }
   }
-  for (int64_t v = (int64_t)kQCache * 32 + lane; v < nvec; v += 32)
+  for (int64_t v = (int64_t)kQCache * kTPR + t; v < nvec; v += kTPR)
     m = fmaxf(m, amax_of(*reinterpret_cast<const uint4*>(x + v * VE), T()));
-  // the row's maximum (max is exact, so the order of the reduction does not matter)
+  // the row's maximum (max is exact, so the order of the reduction does not matter):
+  // lanes of the row's threads within a warp, then the row's warps through shared memory
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  for (int o = (kTPR < 32 ? kTPR : 32) / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if constexpr (kWarpsPerRow > 1) {
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    const int w0 = (threadIdx.x >> 5) / kWarpsPerRow * kWarpsPerRow;
+#pragma unroll
+    for (int w = 0; w < kWarpsPerRow; ++w) m = fmaxf(m, red[w0 + w]);
+  }
+  if (!live) return;
   const float s = __fdiv_rn(fmaxf(m, a.eps), 127.f);
   const float inv = __frcp_rn(s);
   void* q = BF16_CODES ? (void*)(reinterpret_cast<__nv_bfloat16*>(a.q) + row * a.ld_q)
                        : (void*)(reinterpret_cast<int8_t*>(a.q) + row * a.ld_q);
 #pragma unroll
   for (int c = 0; c < kQCache; ++c) {
-    const int64_t v = (int64_t)c * 32 + lane;
+    const int64_t v = (int64_t)c * kTPR + t;
     if (v < nvec) store_codes<T, BF16_CODES>(cache[c], s, inv, q, v);
   }
-  for (int64_t v = (int64_t)kQCache * 32 + lane; v < nvec; v += 32)
+  for (int64_t v = (int64_t)kQCache * kTPR + t; v < nvec; v += kTPR)
     store_codes<T, BF16_CODES>(*reinterpret_cast<const uint4*>(x + v * VE), s, inv, q, v);
-  if (lane == 0) a.scale[row] = s;
+  if (t == 0) a.scale[row] = s;
 }
 
 // ---------------------------------------------------------------------------
