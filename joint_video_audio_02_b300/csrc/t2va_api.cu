@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "t2va_internal.cuh"
+#include "t2va_w8a8.cuh"
 
 using namespace t2va;
 

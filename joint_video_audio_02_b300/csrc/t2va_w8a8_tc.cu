@@ -26,7 +26,7 @@
 // and returns.
 #include <cuda.h>
 
-#include "t2va_internal.cuh"
+#include "t2va_w8a8.cuh"
 
 namespace t2va {
 namespace {
