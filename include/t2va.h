@@ -275,6 +275,14 @@ int t2va_w8a8_linear(int64_t M, int64_t N, int64_t K, t2va_dtype code_dtype, con
                      const float* sx, const void* wq, const float* sw, const float* bias,
                      t2va_dtype out_dtype, void* y, int* status, cudaStream_t stream);
 
+/* Self-test of the tensor-core W8A8 kernel's bounded waits: one 128 x 128 x 128 launch on
+ * library-owned buffers whose MMA thread first waits on an mbarrier that nothing arrives
+ * on. The wait runs out after about a second; the kernel then sets
+ * T2VA_STATUS_TIMEOUT in *status (a device int), drains its copies, frees its TMEM and
+ * returns, and the context stays usable. A tensor-core W8A8 launch given a status word
+ * that already holds T2VA_STATUS_TIMEOUT does nothing, so clear it before reusing it. */
+int t2va_selftest_wait_timeout(int* status, cudaStream_t stream);
+
 /* Bytes of the library's own scratch array used by
  * t2va_stage3_objective_noalloc (1 MiB). Every GPU that loads the library holds
  * this much device memory until the process exits. */

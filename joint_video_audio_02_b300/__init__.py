@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     noise_rf,
     quantize_rows,
     scm_objective,
+    selftest_wait_timeout,
     stage3_objective,
     stage3_objective_cfg,
     stage3_objective_noalloc,

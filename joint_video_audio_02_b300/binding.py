@@ -37,7 +37,7 @@ NOALLOC_SCRATCH_BYTES = 1 << 20   # T2VA_NOALLOC_SCRATCH_BYTES
 EXPORTED = ("t2va_error_string", "t2va_abi_version", "t2va_workspace_bytes", "t2va_workspace_init",
             "t2va_noise", "t2va_scm_objective", "t2va_dmd_objective", "t2va_stage3_objective",
             "t2va_stage3_objective_noalloc", "t2va_noise_rf", "t2va_stage3_objective_cfg",
-            "t2va_quantize_rows", "t2va_w8a8_linear")
+            "t2va_quantize_rows", "t2va_w8a8_linear", "t2va_selftest_wait_timeout")
 
 
 class Segment(ctypes.Structure):
@@ -91,6 +91,8 @@ def _declare(lib):
     lib.t2va_quantize_rows.restype = c_int
     lib.t2va_w8a8_linear.argtypes = [c_int64, c_int64, c_int64, c_int, P, P, P, P, P, c_int, P, P, P]
     lib.t2va_w8a8_linear.restype = c_int
+    lib.t2va_selftest_wait_timeout.argtypes = [P, P]
+    lib.t2va_selftest_wait_timeout.restype = c_int
 
 
 def load(path: Optional[str] = None):
@@ -347,6 +349,12 @@ def w8a8_linear(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.
     _check(load().t2va_w8a8_linear(M, N, K, _code_dtype(xq.dtype), xq.data_ptr(), sx.data_ptr(), wq.data_ptr(),
                                    sw.data_ptr(), _opt(bias), _dtype_code(y.dtype), y.data_ptr(), _opt(status),
                                    _stream(stream)), "t2va_w8a8_linear")
+
+
+def selftest_wait_timeout(status: torch.Tensor, stream=None):
+    """Launch the tensor-core W8A8 kernel's bounded-wait self-test (t2va_selftest_wait_timeout):
+    after about a second `status` holds STATUS_TIMEOUT."""
+    _check(load().t2va_selftest_wait_timeout(status.data_ptr(), _stream(stream)), "t2va_selftest_wait_timeout")
 
 
 def stage3_objective_noalloc(z_t, x0_teacher, x0_student, x0_student_tangent, t, zhat0,

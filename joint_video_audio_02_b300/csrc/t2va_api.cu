@@ -334,7 +334,7 @@ int t2va_w8a8_linear(int64_t M, int64_t N, int64_t K, t2va_dtype code_dtype, con
   if (!aligned(xq, 16) || !aligned(wq, 16) || !aligned(sx, 4) || !aligned(sw, 4) ||
       !aligned(bias, 4) || !aligned(y, tc ? 16 : 8) || !aligned(status, 4))
     return T2VA_ERROR_MISALIGNED;
-  GemmArgs a;
+  GemmArgs a = {};
   a.M = M;
   a.N = N;
   a.K = K;
@@ -348,6 +348,16 @@ int t2va_w8a8_linear(int64_t M, int64_t N, int64_t K, t2va_dtype code_dtype, con
   const cudaError_t e = tc ? launch_w8a8_tc(a, out_dtype == T2VA_BFLOAT16, stream)
                            : launch_w8a8_gemm(a, out_dtype == T2VA_BFLOAT16, stream);
   if (e != cudaSuccess) {
+    cudaGetLastError();
+    return T2VA_ERROR_CUDA;
+  }
+  return T2VA_SUCCESS;
+}
+
+int t2va_selftest_wait_timeout(int* status, cudaStream_t stream) {
+  if (status == nullptr) return T2VA_ERROR_INVALID_ARGUMENT;
+  if (!aligned(status, 4)) return T2VA_ERROR_MISALIGNED;
+  if (launch_w8a8_tc_selftest(status, stream) != cudaSuccess) {
     cudaGetLastError();
     return T2VA_ERROR_CUDA;
   }

@@ -30,11 +30,15 @@ struct GemmArgs {
   const float* bias;           // [N] or null
   void* y;                     // bf16 or float32 [M][N]
   int* status;                 // device status word or null (tensor-core path)
+  int selftest_wait;           // tensor-core path: first wait on a barrier nothing arrives on
 };
 
 cudaError_t launch_quantize_rows(const QuantArgs& a, t2va_dtype dt, cudaStream_t st);
 cudaError_t launch_w8a8_gemm(const GemmArgs& a, bool bf16_out, cudaStream_t st);
 cudaError_t launch_w8a8_tc(const GemmArgs& a, bool bf16_out, cudaStream_t st);
+// One 128 x 128 x 128 tensor-core launch on library-owned buffers whose MMA thread first
+// waits on a barrier that nothing arrives on (a test of the bounded waits).
+cudaError_t launch_w8a8_tc_selftest(int* status, cudaStream_t st);
 int gemm_tile_m();
 int gemm_tile_n();
 int gemm_tile_k();

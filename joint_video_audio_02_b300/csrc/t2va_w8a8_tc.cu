@@ -48,6 +48,7 @@ struct TcSmem {
   uint64_t acc_full[kAccSlots];
   uint64_t acc_empty[kAccSlots];
   uint64_t drain;
+  uint64_t stall;  // never arrived on: the wait of the self-test
   uint32_t tmem_base;
   uint32_t abort;
 };
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(kTThreads, 2)
       mbar_init(&sm.acc_empty[j], 4);
     }
     mbar_init(&sm.drain, 1);
+    mbar_init(&sm.stall, 1);
     sm.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -204,6 +206,10 @@ __global__ void __launch_bounds__(kTThreads, 2)
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      if (a.selftest_wait && !mbar_wait(&sm.stall, 0)) {
+        *abort = 1;
+        if (a.status) atomicOr(a.status, T2VA_STATUS_TIMEOUT);
+      }
       for (int kt = 0; kt < KT && !*abort; ++kt) {
         const int s = kt % kTStages, c = kt / kStagesPerChunk, slot = c % kAccSlots;
         const bool first = (kt % kStagesPerChunk) == 0;
@@ -332,6 +338,30 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K) {
 }
 
 }  // namespace
+
+namespace {
+// buffers of the self-test launch: 128 x 128 bf16 codes (zero), scales, output
+static __device__ __align__(128) __nv_bfloat16 g_st_a[128 * 128];
+static __device__ __align__(128) __nv_bfloat16 g_st_b[128 * 128];
+static __device__ __align__(128) float g_st_y[128 * 128];
+static __device__ float g_st_s[128];
+}  // namespace
+
+cudaError_t launch_w8a8_tc_selftest(int* status, cudaStream_t st) {
+  GemmArgs a = {};
+  a.M = a.N = a.K = 128;
+  void *pa, *pb, *py, *ps;
+  if (cudaGetSymbolAddress(&pa, g_st_a) != cudaSuccess || cudaGetSymbolAddress(&pb, g_st_b) != cudaSuccess ||
+      cudaGetSymbolAddress(&py, g_st_y) != cudaSuccess || cudaGetSymbolAddress(&ps, g_st_s) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  a.xq = reinterpret_cast<const int8_t*>(pa);
+  a.wq = reinterpret_cast<const int8_t*>(pb);
+  a.y = py;
+  a.sx = a.sw = reinterpret_cast<const float*>(ps);
+  a.status = status;
+  a.selftest_wait = 1;
+  return launch_w8a8_tc(a, false, st);
+}
 
 cudaError_t launch_w8a8_tc(const GemmArgs& a, bool bf16_out, cudaStream_t st) {
   CUtensorMap ma, mb;

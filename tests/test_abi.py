@@ -115,6 +115,8 @@ def test_host_validation_without_device(lib):
     assert lib.t2va_w8a8_linear(128, 128, 128, I8, a16, a16, a16, a16, None, 7, a16, None, None) == 2
     assert lib.t2va_w8a8_linear(128, 128, 128, 0, a16, a16, a16, a16, None, 0, a16, None, None) == 2
     assert lib.t2va_w8a8_linear(0, 128, 128, I8, None, None, None, None, None, 0, None, None, None) == 0
+    assert lib.t2va_selftest_wait_timeout(None, None) == 1
+    assert lib.t2va_selftest_wait_timeout(a16 + 2, None) == 3
     # workspace checks come after the argument checks and need no device either
     assert lib.t2va_workspace_init(None, 1024, 0, None) == 4
     assert lib.t2va_workspace_init(ok + 4, 1024, 0, None) == 4

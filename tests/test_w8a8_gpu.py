@@ -10,6 +10,8 @@ y = fma(float(acc), sx * sw, b) rounds float(acc) (once, only past 2^24), sx * s
 fma, so |y - exact| <= 4 * 2^-24 (|sx sw acc| + |b|), plus one output ulp for bfloat16.
 """
 
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -204,3 +206,28 @@ def test_w8a8_guard():
         t2va.w8a8_linear(z, torch.ones(100, device="cuda"), torch.zeros((128, 128), dtype=torch.int8, device="cuda"),
                          torch.ones(128, device="cuda"), torch.empty((100, 128), device="cuda"))
     assert e.value.code == 1
+
+
+def test_bounded_wait_runs_out_and_context_survives():
+    """The tensor-core kernel's waits are bounded: in the self-test launch one wait is on a
+    barrier nothing arrives on. It must end by itself with T2VA_STATUS_TIMEOUT, free its
+    resources, and leave the context usable; a later launch given the flagged status word
+    does nothing, and one given a clear word computes as usual."""
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    t2va.selftest_wait_timeout(st)
+    torch.cuda.synchronize()
+    assert st.item() & t2va.STATUS_TIMEOUT
+    assert time.time() - t0 < 60
+    M = N = K = 128
+    xq, wq = _codes(41, M, K, extreme=True), _codes(42, N, K)
+    one = lambda n: torch.ones(n, device="cuda")
+    y = torch.full((M, N), -1.0, device="cuda")
+    t2va.w8a8_linear(_dev_codes(xq, torch.bfloat16), one(M), _dev_codes(wq, torch.bfloat16), one(N), y, status=st)
+    torch.cuda.synchronize()
+    assert torch.all(y == -1.0)                      # skipped: the word still holds the timeout
+    st.zero_()
+    t2va.w8a8_linear(_dev_codes(xq, torch.bfloat16), one(M), _dev_codes(wq, torch.bfloat16), one(N), y, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(y.cpu().numpy().astype(np.int64), W8.int_dot(xq, wq))
