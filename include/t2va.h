@@ -7,16 +7,20 @@
  * timestep per sample: TrigFlow noising, the joint sCM direction with its
  * per-sample, per-modality L2 normalisation, the DMD term with its
  * residual-scale normaliser, the per-sample losses and the float32 gradients
- * with respect to the student outputs.
+ * with respect to the student outputs. Next to it: the TrigFlow -> rectified-flow
+ * wrapper fused into the noising, the DMD teacher guided per modality, and the
+ * post-scale W8A8 linear of the inference stack.
  *
  * Sources (cited per entry point below):
  *   [zh] "TurboT2VA：分数正则化一致性蒸馏加速 19B 视频音频联合生成，四步采样
  *        20.1×、H20 上全栈 54.67×" (robotworld.top/zh/papers/paper-2608.24674),
- *        sections 三, 3.1, 四, 4.1 (the only page printing the equations).
+ *        sections 三, 3.1, 四, 4.1, 4.2, 6.2, 七 (the only page printing the
+ *        equations).
  *   [en] "TurboT2VA: Score-Regularized Consistency Distillation for Fast
  *        Large-Scale Text-to-Video-Audio Generation"
  *        (robotworld.top/en/papers/paper-2608.24674): Eq. 6 (per-modality L2
- *        normalisation), Eq. 11-12 (DMD residual-scale normaliser).
+ *        normalisation), Eq. 11-12 (DMD residual-scale normaliser), Eq. 16
+ *        (TrigFlow -> rectified-flow wrapper).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -34,8 +38,11 @@
  * - Inputs are float32 or bfloat16 (`dtype`); arithmetic is float32 with
  *   float32 accumulation; gradients are written in float32.
  * - The caller owns every buffer and the stream. The library allocates no
- *   device memory, keeps no state across calls, and never synchronises the
- *   host: calls are asynchronous on `stream`. Outputs must not overlap inputs.
+ *   device memory (it has two static device arrays: the scratch of
+ *   t2va_stage3_objective_noalloc and the buffers of t2va_selftest_wait_timeout),
+ *   keeps no state across calls, and never synchronises the host: calls are
+ *   asynchronous on `stream`. Outputs must not overlap inputs unless an entry
+ *   point says so.
  * - Return value: T2VA_SUCCESS or a synchronous error code (argument checks,
  *   launch failure); nothing is enqueued when an error is returned. Problems
  *   found on the device set bits in the caller's device int `*status`
@@ -74,8 +81,8 @@ typedef struct t2va_segment {
 enum {
   T2VA_SUCCESS = 0,
   T2VA_ERROR_INVALID_ARGUMENT = 1,  /* bad size, scalar or null pointer          */
-  T2VA_ERROR_UNSUPPORTED_DTYPE = 2, /* dtype is not T2VA_FLOAT32/T2VA_BFLOAT16     */
-  T2VA_ERROR_MISALIGNED = 3,        /* a device pointer is not 16-byte aligned     */
+  T2VA_ERROR_UNSUPPORTED_DTYPE = 2, /* a dtype the entry point does not take        */
+  T2VA_ERROR_MISALIGNED = 3,        /* a device pointer breaks its alignment rule  */
   T2VA_ERROR_WORKSPACE = 4,         /* workspace null, misaligned or too small     */
   T2VA_ERROR_CUDA = 5               /* a CUDA runtime call or launch failed        */
 };
@@ -96,7 +103,8 @@ int t2va_abi_version(void);
 
 /* Bytes of workspace needed by the objective entry points for up to `batch`
  * samples of `num_modalities` modalities: 256 bytes plus 16 KiB per (sample,
- * modality). An objective call is two kernels on `stream`; the first writes
+ * modality). An objective call is two kernels on `stream` (both programmatic
+ * dependents of the work before them); the first writes
  * per-chunk partial sums into the workspace and the second reads them, so the
  * workspace needs no initialisation and keeps nothing between calls. Calls that
  * may run concurrently need distinct workspaces. Returns 0 on invalid arguments
@@ -250,8 +258,8 @@ int t2va_stage3_objective_cfg(
  * weight matrix (rows = output channels). Requires eps > 0, cols a multiple of 16
  * bytes of input (8 bf16 or 4 float32 elements), ld_x * element size a multiple of 16,
  * ld_q a multiple of the codes written per input vector (16 / element size), x and q
- * 16-byte aligned. One warp per row: reads each input once (rows longer than 8 KiB are
- * read a second time, from L2). One kernel on `stream`. */
+ * 16-byte aligned. 128 threads per row: reads each input once (rows longer than 8 KiB
+ * are read a second time, from L2). One kernel on `stream`. */
 int t2va_quantize_rows(int64_t rows, int64_t cols, t2va_dtype dtype, const void* x, int64_t ld_x,
                        float eps, t2va_dtype code_dtype, void* q, int64_t ld_q, float* scale,
                        cudaStream_t stream);
