@@ -84,3 +84,24 @@ def test_cfg_bad_timestep_and_guidance_errors():
                                   lambda_scm=1, lambda_dmd=1, grad_x0_student=g, grad_zhat0=g,
                                   loss=loss, workspace=ws, status=st)
     assert e.value.code == 1
+
+
+def test_cfg_accumulate_and_alias():
+    """The guided objective accumulates into existing gradients, and sums both gradients
+    into one buffer when grad_zhat0 is grad_x0_student, as the plain stage-3 call does."""
+    inp = S.make_inputs(2, [20000, 333], "bf16", S.STAGE3_CFG, seed=(603,))
+    p = Params(guidance=(2.0, 4.5))
+    rng = np.random.default_rng(1)
+    prior = {"grad_x0_student": [rng.normal(size=a.shape).astype(np.float32) for a in inp.z0],
+             "grad_zhat0": [rng.normal(size=a.shape).astype(np.float32) for a in inp.z0]}
+    gpu = gpu_run(inp, p, S.STAGE3_CFG, accumulate_into=prior)
+    ref = oracle_run(inp, p, S.STAGE3_CFG)
+    for k in ("grad_x0_student", "grad_zhat0"):
+        ref[k] = [r + q.astype(np.float64) for r, q in zip(ref[k], prior[k])]
+    compare(gpu, ref, "bf16", S.STAGE3_CFG)
+    gpu = gpu_run(inp, p, S.STAGE3_CFG, alias=True)
+    ref = oracle_run(inp, p, S.STAGE3_CFG)
+    summed = [a + b for a, b in zip(ref["grad_x0_student"], ref["grad_zhat0"])]
+    ref["grad_x0_student"] = summed
+    ref["grad_zhat0"] = summed
+    compare(gpu, ref, "bf16", S.STAGE3_CFG)
