@@ -61,7 +61,7 @@
 extern "C" {
 #endif
 
-#define T2VA_ABI_VERSION 1
+#define T2VA_ABI_VERSION 2  /* 2: t2va_noise_rf, t2va_stage3_objective_cfg, the W8A8 entry points */
 #define T2VA_MAX_MODALITIES 4
 
 typedef enum t2va_dtype {
