@@ -8,13 +8,14 @@
  * per-sample, per-modality L2 normalisation, the DMD term with its
  * residual-scale normaliser, the per-sample losses and the float32 gradients
  * with respect to the student outputs. Next to it: the TrigFlow -> rectified-flow
- * wrapper fused into the noising, the DMD teacher guided per modality, and the
- * post-scale W8A8 linear of the inference stack.
+ * wrapper fused into the noising, the DMD teacher guided per modality, and from the
+ * inference stack the post-scale W8A8 linear and the fused residual + modulated RMS
+ * normalisation.
  *
  * Sources (cited per entry point below):
  *   [zh] "TurboT2VA：分数正则化一致性蒸馏加速 19B 视频音频联合生成，四步采样
  *        20.1×、H20 上全栈 54.67×" (robotworld.top/zh/papers/paper-2608.24674),
- *        sections 三, 3.1, 四, 4.1, 4.2, 6.2, 七 (the only page printing the
+ *        sections 三, 3.1, 四, 4.1, 4.2, 6.2, 6.3, 七 (the only page printing the
  *        equations).
  *   [en] "TurboT2VA: Score-Regularized Consistency Distillation for Fast
  *        Large-Scale Text-to-Video-Audio Generation"
@@ -61,7 +62,7 @@
 extern "C" {
 #endif
 
-#define T2VA_ABI_VERSION 2  /* 2: t2va_noise_rf, t2va_stage3_objective_cfg, the W8A8 entry points */
+#define T2VA_ABI_VERSION 2  /* 2: t2va_noise_rf, t2va_stage3_objective_cfg, W8A8, t2va_residual_modnorm */
 #define T2VA_MAX_MODALITIES 4
 
 typedef enum t2va_dtype {
@@ -282,6 +283,24 @@ int t2va_quantize_rows(int64_t rows, int64_t cols, t2va_dtype dtype, const void*
 int t2va_w8a8_linear(int64_t M, int64_t N, int64_t K, t2va_dtype code_dtype, const void* xq,
                      const float* sx, const void* wq, const float* sw, const float* bias,
                      t2va_dtype out_dtype, void* y, int* status, cudaStream_t stream);
+
+/* Fused gated residual update + modulated RMS normalisation  ([zh] 6.3: the joint
+ * Transformer combines a normalisation with a modality- and timestep-dependent
+ * modulation, then a gated residual update; the pages print no formulas, and the
+ * standard diffusion-Transformer forms are taken). Per token row r of D contiguous
+ * elements, with sample b = r / rows_per_sample:
+ *   h'[r] = h[r] + gate[b] * u[r]                          (if u is given; else h' = h)
+ *   y[r]  = h'[r] / sqrt(mean(h'[r]^2) + eps) * (1 + scale[b]) + shift[b]
+ * h' is rounded to `dtype` and the normalisation uses the rounded values. gate, scale
+ * and shift are float32 [samples][D] device arrays, each may be NULL (gate 1, scale 0,
+ * shift 0; gate only with u). h' is stored in `h_out` if it is not NULL (h_out may be
+ * h, an in-place update; it needs u). y may not be h, u or h_out. Requires D a multiple
+ * of 16 bytes of elements, rows_per_sample >= 1, eps >= 0, every pointer 16-byte
+ * aligned. One kernel on `stream`, 128 threads per row; reads h (and u) once and writes
+ * h' and y once. */
+int t2va_residual_modnorm(int64_t rows, int64_t D, int64_t rows_per_sample, t2va_dtype dtype,
+                          const void* h, const void* u, const float* gate, const float* scale,
+                          const float* shift, float eps, void* h_out, void* y, cudaStream_t stream);
 
 /* Self-test of the tensor-core W8A8 kernel's bounded waits: one 128 x 128 x 128 launch on
  * library-owned buffers whose MMA thread first waits on an mbarrier that nothing arrives

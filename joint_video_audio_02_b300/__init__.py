@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     noise,
     noise_rf,
     quantize_rows,
+    residual_modnorm,
     scm_objective,
     selftest_wait_timeout,
     stage3_objective,

@@ -37,7 +37,8 @@ NOALLOC_SCRATCH_BYTES = 1 << 20   # T2VA_NOALLOC_SCRATCH_BYTES
 EXPORTED = ("t2va_error_string", "t2va_abi_version", "t2va_workspace_bytes", "t2va_workspace_init",
             "t2va_noise", "t2va_scm_objective", "t2va_dmd_objective", "t2va_stage3_objective",
             "t2va_stage3_objective_noalloc", "t2va_noise_rf", "t2va_stage3_objective_cfg",
-            "t2va_quantize_rows", "t2va_w8a8_linear", "t2va_selftest_wait_timeout")
+            "t2va_quantize_rows", "t2va_w8a8_linear", "t2va_selftest_wait_timeout",
+            "t2va_residual_modnorm")
 
 
 class Segment(ctypes.Structure):
@@ -93,6 +94,8 @@ def _declare(lib):
     lib.t2va_w8a8_linear.restype = c_int
     lib.t2va_selftest_wait_timeout.argtypes = [P, P]
     lib.t2va_selftest_wait_timeout.restype = c_int
+    lib.t2va_residual_modnorm.argtypes = [c_int64, c_int64, c_int64, c_int, P, P, P, P, P, c_float, P, P, P]
+    lib.t2va_residual_modnorm.restype = c_int
 
 
 def load(path: Optional[str] = None):
@@ -349,6 +352,28 @@ def w8a8_linear(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.
     _check(load().t2va_w8a8_linear(M, N, K, _code_dtype(xq.dtype), xq.data_ptr(), sx.data_ptr(), wq.data_ptr(),
                                    sw.data_ptr(), _opt(bias), _dtype_code(y.dtype), y.data_ptr(), _opt(status),
                                    _stream(stream)), "t2va_w8a8_linear")
+
+
+def residual_modnorm(h: torch.Tensor, y: torch.Tensor, *, u: Optional[torch.Tensor] = None,
+                     gate: Optional[torch.Tensor] = None, scale: Optional[torch.Tensor] = None,
+                     shift: Optional[torch.Tensor] = None, eps: float = 1e-6,
+                     h_out: Optional[torch.Tensor] = None, rows_per_sample: Optional[int] = None,
+                     stream=None):
+    """Fused gated residual + modulated RMS normalisation (t2va_residual_modnorm) over token
+    rows: h [rows, D] (and u, h_out, y of that shape, contiguous, one dtype); gate, scale,
+    shift float32 [samples, D]; row r belongs to sample r // rows_per_sample (default: all
+    rows one sample)."""
+    rows, D = int(h.shape[0]), int(h.shape[1])
+    for t in [h, y] + [x for x in (u, h_out) if x is not None]:
+        if tuple(t.shape) != (rows, D) or not t.is_contiguous() or t.dtype != h.dtype:
+            raise ValueError("h, u, h_out and y must be contiguous [rows, D] of one dtype")
+    for name, v in (("gate", gate), ("scale", scale), ("shift", shift)):
+        if v is not None:
+            _f32(v, name)
+    rps = rows if rows_per_sample is None else int(rows_per_sample)
+    _check(load().t2va_residual_modnorm(rows, D, max(1, rps), _dtype_code(h.dtype), h.data_ptr(), _opt(u),
+                                        _opt(gate), _opt(scale), _opt(shift), float(eps), _opt(h_out),
+                                        y.data_ptr(), _stream(stream)), "t2va_residual_modnorm")
 
 
 def selftest_wait_timeout(status: torch.Tensor, stream=None):

@@ -10,7 +10,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libt2va.so")
 SOURCES = ["t2va_api.cu", "t2va_noise.cu", "t2va_objective.cu", "t2va_noalloc.cu", "t2va_w8a8.cu",
-           "t2va_w8a8_tc.cu"]
+           "t2va_w8a8_tc.cu", "t2va_fused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

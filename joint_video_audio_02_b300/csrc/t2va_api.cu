@@ -9,6 +9,7 @@
 
 #include "t2va_internal.cuh"
 #include "t2va_w8a8.cuh"
+#include "t2va_fused.cuh"
 
 using namespace t2va;
 
@@ -348,6 +349,45 @@ int t2va_w8a8_linear(int64_t M, int64_t N, int64_t K, t2va_dtype code_dtype, con
   const cudaError_t e = tc ? launch_w8a8_tc(a, out_dtype == T2VA_BFLOAT16, stream)
                            : launch_w8a8_gemm(a, out_dtype == T2VA_BFLOAT16, stream);
   if (e != cudaSuccess) {
+    cudaGetLastError();
+    return T2VA_ERROR_CUDA;
+  }
+  return T2VA_SUCCESS;
+}
+
+int t2va_residual_modnorm(int64_t rows, int64_t D, int64_t rows_per_sample, t2va_dtype dtype,
+                          const void* h, const void* u, const float* gate, const float* scale,
+                          const float* shift, float eps, void* h_out, void* y, cudaStream_t stream) {
+  T2VA_TRY(check_dtype(dtype));
+  const int esz = dtype == T2VA_BFLOAT16 ? 2 : 4;
+  if (rows < 0 || D < 0 || rows_per_sample < 1 || rows > (int64_t)INT32_MAX * 2 || !finite(eps) ||
+      !(eps >= 0.f))
+    return T2VA_ERROR_INVALID_ARGUMENT;
+  if (rows == 0 || D == 0) return T2VA_SUCCESS;
+  if (h == nullptr || y == nullptr) return T2VA_ERROR_INVALID_ARGUMENT;
+  // rows of whole 16-byte vectors; the per-sample vectors are read 4 floats at a time
+  if (D % (16 / esz) != 0) return T2VA_ERROR_INVALID_ARGUMENT;
+  // without a residual update there is no h' to store and no gate
+  if (u == nullptr && (h_out != nullptr || gate != nullptr)) return T2VA_ERROR_INVALID_ARGUMENT;
+  // y is written after its row is read: it may not be an input or h'
+  if (y == h || y == u || (h_out != nullptr && (y == h_out || h_out == u))) return T2VA_ERROR_INVALID_ARGUMENT;
+  for (const void* p : {h, u, static_cast<const void*>(h_out), static_cast<const void*>(y),
+                        static_cast<const void*>(gate), static_cast<const void*>(scale),
+                        static_cast<const void*>(shift)})
+    if (!aligned(p, 16)) return T2VA_ERROR_MISALIGNED;
+  FusedArgs a;
+  a.rows = rows;
+  a.D = D;
+  a.rows_per_sample = rows_per_sample;
+  a.h = h;
+  a.u = u;
+  a.gate = gate;
+  a.scale = scale;
+  a.shift = shift;
+  a.eps = eps;
+  a.h_out = h_out;
+  a.y = y;
+  if (launch_residual_modnorm(a, dtype, stream) != cudaSuccess) {
     cudaGetLastError();
     return T2VA_ERROR_CUDA;
   }

@@ -115,6 +115,16 @@ def test_host_validation_without_device(lib):
     assert lib.t2va_w8a8_linear(128, 128, 128, I8, a16, a16, a16, a16, None, 7, a16, None, None) == 2
     assert lib.t2va_w8a8_linear(128, 128, 128, 0, a16, a16, a16, a16, None, 0, a16, None, None) == 2
     assert lib.t2va_w8a8_linear(0, 128, 128, I8, None, None, None, None, None, 0, None, None, None) == 0
+    # the fused residual + modulated normalisation
+    assert lib.t2va_residual_modnorm(4, 100, 1, 1, a16, a16, None, None, None, 1e-6, None, a16 + 64, None) == 1  # D % 8
+    assert lib.t2va_residual_modnorm(4, 128, 0, 1, a16, a16, None, None, None, 1e-6, None, a16 + 64, None) == 1  # rows/sample
+    assert lib.t2va_residual_modnorm(4, 128, 1, 1, a16, None, a16, None, None, 1e-6, None, a16 + 64, None) == 1  # gate w/o u
+    assert lib.t2va_residual_modnorm(4, 128, 1, 1, a16, None, None, None, None, 1e-6, a16, a16 + 64, None) == 1  # h' w/o u
+    assert lib.t2va_residual_modnorm(4, 128, 1, 1, a16, a16 + 32, None, None, None, 1e-6, None, a16, None) == 1  # y is h
+    assert lib.t2va_residual_modnorm(4, 128, 1, 1, a16, None, None, None, None, -1.0, None, a16 + 64, None) == 1
+    assert lib.t2va_residual_modnorm(4, 128, 1, 1, a16 + 8, None, None, None, None, 1e-6, None, a16 + 64, None) == 3
+    assert lib.t2va_residual_modnorm(4, 128, 1, 5, a16, None, None, None, None, 1e-6, None, a16 + 64, None) == 2
+    assert lib.t2va_residual_modnorm(0, 128, 1, 1, None, None, None, None, None, 1e-6, None, None, None) == 0
     assert lib.t2va_selftest_wait_timeout(None, None) == 1
     assert lib.t2va_selftest_wait_timeout(a16 + 2, None) == 3
     # workspace checks come after the argument checks and need no device either
