@@ -1,7 +1,9 @@
-"""CPU oracle (float64, numpy) for the joint video-audio sCM + DMD objective.
+"""CPU oracles (float64, numpy) for the joint video-audio sCM + DMD objective
+(t2va_oracle), the post-scale W8A8 linear (w8a8_oracle) and the fused gated residual +
+modulated RMS normalisation (fused_ops_oracle).
 
 TEST INFRASTRUCTURE ONLY: imported by the test suite, the smoke check and the
-benchmark's CPU-baseline leg. The CUDA library never uses it.
+benchmark's CPU legs. The CUDA library never uses them.
 """
 
 from .t2va_oracle import (  # noqa: F401
