@@ -536,10 +536,12 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
 
 def run_e2e(args, wl, host0, dsets, status, noise, objective, dev, nb, world, dist):
     """The same steps with host buffers: every step copies its inputs in from pinned host
-    memory and its gradients and losses back out. Steps are pipelined the way a data
-    loader feeds a training loop: two device buffer sets alternate, and the copies in,
-    the compute and the copies out run on three streams ordered by events, so step i+1's
-    inputs arrive while step i computes and step i-1's results drain."""
+    memory and reads its result, the per-sample losses, back to the host (the gradients
+    stay on the device, where the networks' backward pass consumes them). Steps are
+    pipelined the way a data loader feeds a training loop: two device buffer sets
+    alternate, and the copies in, the compute and the copies out run on three streams
+    ordered by events, so step i+1's inputs arrive while step i computes and step i-1's
+    result drains."""
     import torch
 
     steps = max(4, min(args.steps, args.e2e_steps))
@@ -557,7 +559,7 @@ def run_e2e(args, wl, host0, dsets, status, noise, objective, dev, nb, world, di
                 ts = [torch.from_numpy(a).pin_memory() for a in arrs]
         pinned[f] = ts
         h2d += sum(x.numel() * x.element_size() for x in ts)
-    outs = ["gS", "loss"] + (["gD"] if is_stage3(wl) else [])
+    outs = ["loss"]
 
     def as_list(v):
         return v if isinstance(v, list) else [v]
@@ -612,7 +614,8 @@ def run_e2e(args, wl, host0, dsets, status, noise, objective, dev, nb, world, di
     return {"value": round(whole_job_gbs(world, nb["step"], steps, ms), 3), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": ms / steps,
-            "pipeline": "2 device buffer sets; copy-in, compute and copy-out streams"}
+            "pipeline": "2 device buffer sets; copy-in, compute and copy-out streams",
+            "read_back": "per-sample losses (the gradients stay on the device)"}
 
 
 # ---------------------------------------------------------------------------
