@@ -294,7 +294,9 @@ __device__ __forceinline__ void scalar_direction(const ObjectiveArgs& a, int m, 
 }
 
 // Eight consecutive gradients (32 bytes, 32-byte aligned) in one store, so every
-// store instruction of a warp writes whole 32-byte sectors.
+// store instruction of a warp writes whole 32-byte sectors. The lines are marked first
+// to leave L2 (the gradients are not read again here), which keeps the inputs that the
+// second pass re-reads resident; measured faster than a streaming (.cs) store.
 __device__ __forceinline__ void write8(float* dst, const float* v, int accumulate) {
   float o[8];
 #pragma unroll
@@ -305,8 +307,9 @@ __device__ __forceinline__ void write8(float* dst, const float* v, int accumulat
     o[0] += a0.x; o[1] += a0.y; o[2] += a0.z; o[3] += a0.w;
     o[4] += a1.x; o[5] += a1.y; o[6] += a1.z; o[7] += a1.w;
   }
-  asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "f"(o[0]),
-               "f"(o[1]), "f"(o[2]), "f"(o[3]), "f"(o[4]), "f"(o[5]), "f"(o[6]), "f"(o[7])
+  asm volatile("st.global.L2::cache_hint.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8}, %9;" ::"l"(dst),
+               "f"(o[0]), "f"(o[1]), "f"(o[2]), "f"(o[3]), "f"(o[4]), "f"(o[5]), "f"(o[6]), "f"(o[7]),
+               "l"(policy_evict_first())
                : "memory");
 }
 
