@@ -859,7 +859,8 @@ def run_w8a8(args, name: str):
                    "l2": "activations 235 MB / 50 MB and outputs larger than L2 at M = 28672 / 6144; "
                          "the 16.8 MB int8 weights stay in L2 by design",
                    "timing": "CUDA graphs of back-to-back steps, CUDA events on the launching stream"},
-        "roofline": {"kernel": "k_w8a8_tc (tcgen05.mma kind::f16, TMA, TMEM)" if codes == "bf16"
+        "roofline": {"kernel": ("k_w8a8_tc_wide (tcgen05.mma kind::f16 M128 N256, TMA, TMEM)" if N % 256 == 0
+                                else "k_w8a8_tc (tcgen05.mma kind::f16 M128 N128, TMA, TMEM)") if codes == "bf16"
                                else "k_w8a8_gemm (mma.sync m16n8k32 s8)", "bound": "tensor",
                      "achieved": round(flops / (ms_l * 1e-3) / 1e12, 2), "peak": peak_bf16,
                      "unit": "TOPS", "frac": round(flops / (ms_l * 1e-3) / 1e12 / peak_bf16, 4),

@@ -276,8 +276,9 @@ int t2va_quantize_rows(int64_t rows, int64_t cols, t2va_dtype dtype, const void*
  *     INT8 form of the fifth-generation tensor-core MMA.
  *   - T2VA_BFLOAT16 codes: tcgen05.mma (bf16 x bf16 -> f32 in TMEM), K summed in chunks
  *     of 1024 whose float32 sums stay below 2^24 and are therefore exact integers, the
- *     chunks added as int32. Same result, at the bf16 tensor-core rate. Needs y 16-byte
- *     aligned. Its pipeline waits are bounded: a wait that runs out sets
+ *     chunks added as int32. Same result, at the bf16 tensor-core rate: 128 x 256 tiles
+ *     on one persistent CTA per SM when N is a multiple of 256, else 128 x 128 tiles.
+ *     Needs y 16-byte aligned. Its pipeline waits are bounded: a wait that runs out sets
  *     T2VA_STATUS_TIMEOUT in `status` (may be NULL) and leaves y incomplete.
  * One kernel on `stream`. */
 int t2va_w8a8_linear(int64_t M, int64_t N, int64_t K, t2va_dtype code_dtype, const void* xq,

@@ -10,8 +10,10 @@
 // whatever the order of the additions, and the chunks are added as int32 by the
 // epilogue. The result is the exact INT32 sum of the pages' operator.
 //
-// One CTA per 128 x 128 output tile, 192 threads, two CTAs per SM (one CTA's epilogue and
-// set-up overlap the other's MMAs; measured 591 -> 903 TOPS at 28672 x 4096 x 4096):
+// Two kernels. When N is a multiple of 256, k_w8a8_tc_wide (below) runs persistent CTAs
+// over 128 x 256 tiles. Otherwise k_w8a8_tc runs one CTA per 128 x 128 output tile, 192
+// threads, two CTAs per SM (one CTA's epilogue and set-up overlap the other's MMAs;
+// measured 591 -> 903 TOPS at 28672 x 4096 x 4096):
 //   warp 0      TMA producer: A and B tiles of 128 rows x 64 bf16 (128 bytes, swizzled
 //               128B) into a 3-stage shared-memory ring, one mbarrier per stage;
 //   warp 1      allocates 256 TMEM columns (two 128-column float32 accumulators)
@@ -101,10 +103,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTN >> 3) << 17) |
                             ((uint32_t)(kTM >> 4) << 24);
 
-__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t accumulate) {
+// Instruction descriptor of the wide tiles: M = 128, N = 256.
+constexpr int kWN = 256;
+constexpr uint32_t kIdescWide = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kWN >> 3) << 17) |
+                                ((uint32_t)(kTM >> 4) << 24);
+
+__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t accumulate,
+                                     uint32_t idesc = kIdesc) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -304,6 +312,224 @@ __global__ void __launch_bounds__(kTThreads, 2)
   }
 }
 
+// Wide tiles (N divisible by 256): one persistent CTA per SM walks output tiles of
+// 128 x 256, tile t at rows 128 (t / (N / 256)) and columns 256 (t % (N / 256)), so the
+// CTAs running at once share A row blocks and all of B through L2. An M128 N256 K16 MMA
+// reads 12 KB of operands from shared memory per 128 tensor-core cycles, against 8 KB per
+// 64 cycles for N = 128, so the shared-memory traffic of the operands (TMA writes plus MMA
+// reads) per flop falls by a quarter (measured 1141 -> 1370 TOPS at 28672 x 4096 x 4096).
+// 320 threads:
+//   warp 0      TMA producer: per stage one 128 x 64 A box and two 128 x 64 B boxes (the
+//               B tile's rows 0-127 and 128-255, contiguous in shared memory), 4 stages;
+//   warp 1      allocates all 512 TMEM columns (two 256-column float32 accumulators,
+//               used as a ring across chunks and tiles) and issues 4 x (M128 N256 K16)
+//               per stage;
+//   warps 2-9   epilogue: two warps per TMEM lane quadrant (rows), one per 128-column
+//               half; they add each finished chunk as int32 and write the tile's y once,
+//               while the MMAs of the next chunk, or of the next tile, proceed in the
+//               other accumulator.
+constexpr int kWStages = 4;
+constexpr int kWEpiWarps = 8;
+constexpr int kWThreads = 64 + 32 * kWEpiWarps;
+constexpr int kWTmemCols = 2 * kWN;
+constexpr uint32_t kWStageTx = kTileBytes + 2 * kTileBytes;   // A 16 KB + B 32 KB
+constexpr size_t kWSmem = 1024 /* alignment slack */ + (size_t)kWStages * kWStageTx + 1024;
+
+struct WideSmem {
+  uint64_t full[kWStages];
+  uint64_t empty[kWStages];
+  uint64_t acc_full[kAccSlots];
+  uint64_t acc_empty[kAccSlots];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort;
+};
+
+template <bool BF16_OUT>
+__global__ void __launch_bounds__(kWThreads, 1)
+    k_w8a8_tc_wide(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                   const __grid_constant__ GemmArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = su32(smem_raw);
+  const uint32_t tiles = (raw + 1023u) & ~1023u;
+  WideSmem& sm = *reinterpret_cast<WideSmem*>(smem_raw + (tiles - raw) + kWStages * kWStageTx);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KT = (int)(a.K / kTK);
+  const int nchunks = (KT + kStagesPerChunk - 1) / kStagesPerChunk;
+  const int tiles_n = (int)(a.N / kWN);
+  const int ntiles = (int)(a.M / kTM) * tiles_n;
+
+  __shared__ uint32_t skip;
+  if (threadIdx.x == 0)
+    skip = (a.status != nullptr && (*reinterpret_cast<volatile int*>(a.status) & T2VA_STATUS_TIMEOUT)) ? 1u : 0u;
+  __syncthreads();
+  if (skip) return;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int j = 0; j < kAccSlots; ++j) {
+      mbar_init(&sm.acc_full[j], 1);
+      mbar_init(&sm.acc_empty[j], kWEpiWarps);
+    }
+    mbar_init(&sm.drain, 1);
+    sm.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&sm.tmem_base)),
+                 "r"(kWTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  volatile uint32_t* abort = &sm.abort;
+  if (warp == 0) {
+    if (lane == 0) {
+      int64_t g = 0, issued = 0;  // stages over all of this CTA's tiles
+      for (int tile = blockIdx.x; tile < ntiles && !*abort; tile += gridDim.x) {
+        const int m0 = (tile / tiles_n) * kTM, n0 = (tile % tiles_n) * kWN;
+        for (int kt = 0; kt < KT && !*abort; ++kt, ++g) {
+          const int s = (int)(g % kWStages);
+          const int64_t use = g / kWStages;
+          if (use > 0 && !mbar_wait(&sm.empty[s], (uint32_t)((use - 1) & 1))) {
+            *abort = 1;
+            if (a.status) atomicOr(a.status, T2VA_STATUS_TIMEOUT);
+            break;
+          }
+          const uint32_t sa = tiles + s * kWStageTx;
+          mbar_expect_tx(&sm.full[s], kWStageTx);
+          tma_2d(sa, &map_a, &sm.full[s], kt * kTK, m0);
+          tma_2d(sa + kTileBytes, &map_b, &sm.full[s], kt * kTK, n0);
+          tma_2d(sa + 2 * kTileBytes, &map_b, &sm.full[s], kt * kTK, n0 + kTM);
+          issued = g + 1;
+        }
+      }
+      // every copy this thread started has landed before the CTA's shared memory goes
+      for (int64_t q = issued > kWStages ? issued - kWStages : 0; q < issued; ++q)
+        mbar_wait(&sm.full[q % kWStages], (uint32_t)((q / kWStages) & 1));
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int64_t g = 0, gc0 = 0;  // stages and chunks over all of this CTA's tiles
+      bool dead = false;
+      for (int tile = blockIdx.x; tile < ntiles && !dead; tile += gridDim.x, gc0 += nchunks) {
+        for (int kt = 0; kt < KT; ++kt, ++g) {
+          if (*abort) {
+            dead = true;
+            break;
+          }
+          const int s = (int)(g % kWStages);
+          const int64_t gc = gc0 + kt / kStagesPerChunk;
+          const int slot = (int)(gc % kAccSlots);
+          const bool first = (kt % kStagesPerChunk) == 0;
+          if (first && gc >= kAccSlots) {
+            if (!mbar_wait(&sm.acc_empty[slot], (uint32_t)(((gc / kAccSlots) - 1) & 1))) {
+              *abort = 1;
+              if (a.status) atomicOr(a.status, T2VA_STATUS_TIMEOUT);
+              dead = true;
+              break;
+            }
+            tc_fence_after();
+          }
+          if (!mbar_wait(&sm.full[s], (uint32_t)((g / kWStages) & 1))) {
+            *abort = 1;
+            if (a.status) atomicOr(a.status, T2VA_STATUS_TIMEOUT);
+            dead = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = tiles + s * kWStageTx;
+          const uint64_t da = smem_desc(sa), db = smem_desc(sa + kTileBytes);
+#pragma unroll
+          for (int k = 0; k < kTK / 16; ++k)
+            umma(tmem + slot * kWN, da + (uint64_t)(k * 2), db + (uint64_t)(k * 2), (first && k == 0) ? 0u : 1u,
+                 kIdescWide);
+          umma_commit(&sm.empty[s]);
+          if ((kt % kStagesPerChunk) == kStagesPerChunk - 1 || kt == KT - 1) umma_commit(&sm.acc_full[slot]);
+        }
+      }
+      umma_commit(&sm.drain);
+      mbar_wait(&sm.drain, 0);
+    }
+  } else {
+    // warp w reads TMEM lanes 32 (w % 4) .. + 31 (rows), columns 128 h .. + 127
+    const int g = warp & 3, h = (warp - 2) >> 2;
+    const uint32_t lane_base = (uint32_t)(32 * g) << 16;
+    int64_t gc = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      const int64_t m0 = (int64_t)(tile / tiles_n) * kTM, n0 = (int64_t)(tile % tiles_n) * kWN + h * kTN;
+      int acc[kTN];
+#pragma unroll
+      for (int j = 0; j < kTN; ++j) acc[j] = 0;
+      for (int c = 0; c < nchunks; ++c, ++gc) {
+        const int slot = (int)(gc % kAccSlots);
+        if (!mbar_wait(&sm.acc_full[slot], (uint32_t)((gc / kAccSlots) & 1))) {
+          ok = false;
+          *abort = 1;
+          if (a.status) atomicOr(a.status, T2VA_STATUS_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < kTN / 32; ++q) {
+          float v[32];
+          tmem_ld32(tmem + lane_base + slot * kWN + h * kTN + q * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[q * 32 + i] += __float2int_rn(v[i]);  // exact integers
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_empty[slot]);
+      }
+      if (!ok) break;
+      const int64_t row = m0 + 32 * g + lane;
+      const float sx = __ldg(a.sx + row);
+#pragma unroll
+      for (int q = 0; q < kTN / 8; ++q) {
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int64_t col = n0 + q * 8 + i;
+          const float b = a.bias ? __ldg(a.bias + col) : 0.f;
+          y[i] = fmaf((float)acc[q * 8 + i], sx * __ldg(a.sw + col), b);
+        }
+        if constexpr (BF16_OUT) {
+          uint4 o;
+          __nv_bfloat162 h0 = __floats2bfloat162_rn(y[0], y[1]), h1 = __floats2bfloat162_rn(y[2], y[3]);
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(y[4], y[5]), h3 = __floats2bfloat162_rn(y[6], y[7]);
+          o.x = *reinterpret_cast<uint32_t*>(&h0);
+          o.y = *reinterpret_cast<uint32_t*>(&h1);
+          o.z = *reinterpret_cast<uint32_t*>(&h2);
+          o.w = *reinterpret_cast<uint32_t*>(&h3);
+          *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) + row * a.N + n0 + q * 8) = o;
+        } else {
+          float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) + row * a.N + n0 + q * 8);
+          d[0] = make_float4(y[0], y[1], y[2], y[3]);
+          d[1] = make_float4(y[4], y[5], y[6], y[7]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kWTmemCols) : "memory");
+  }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -363,9 +589,42 @@ cudaError_t launch_w8a8_tc_selftest(int* status, cudaStream_t st) {
   return launch_w8a8_tc(a, false, st);
 }
 
+// The wide persistent kernel: one CTA per SM (its shared memory admits no second one),
+// at most one per tile.
+static cudaError_t launch_w8a8_tc_wide(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a, bool bf16_out,
+                                cudaStream_t st) {
+  static bool attr_done = false;
+  static int sms = 0;
+  if (!attr_done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_w8a8_tc_wide<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_w8a8_tc_wide<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWSmem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int64_t ntiles = (a.M / kTM) * (a.N / kWN);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(ntiles < sms ? ntiles : sms));
+  cfg.blockDim = dim3(kWThreads);
+  cfg.dynamicSmemBytes = kWSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (bf16_out) return cudaLaunchKernelEx(&cfg, k_w8a8_tc_wide<true>, ma, mb, a);
+  return cudaLaunchKernelEx(&cfg, k_w8a8_tc_wide<false>, ma, mb, a);
+}
+
 cudaError_t launch_w8a8_tc(const GemmArgs& a, bool bf16_out, cudaStream_t st) {
   CUtensorMap ma, mb;
   if (!make_map(&ma, a.xq, a.M, a.K) || !make_map(&mb, a.wq, a.N, a.K)) return cudaErrorInvalidValue;
+  if (a.N % kWN == 0 && !a.selftest_wait) return launch_w8a8_tc_wide(ma, mb, a, bf16_out, st);
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(k_w8a8_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);

@@ -148,6 +148,31 @@ def test_w8a8_linear_parity(code, out_dtype, M, N, K, bias):
     _check_linear(y.float().cpu().numpy(), acc, sx, sw, b, out_dtype)
 
 
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_w8a8_wide_tiles_more_than_one_per_sm(out_dtype):
+    """N divisible by 256 takes the persistent 128 x 256 tensor-core kernel. 20 x 8 = 160
+    tiles on at most 148 CTAs: some CTAs run two tiles, their accumulators continuing the
+    ring across tiles, and K = 1152 ends each tile with a partial chunk. Rows sampled in
+    every TMEM lane quadrant of every row tile, all columns (both halves of each tile),
+    against the oracle's exact sums."""
+    M, N, K = 2560, 2048, 1152
+    xq = _codes(71, M, K, extreme=True)
+    wq = _codes(72, N, K, extreme=True)
+    r = np.random.default_rng(73)
+    sx = r.uniform(1e-4, 0.05, M).astype(np.float32)
+    sw = r.uniform(1e-4, 0.05, N).astype(np.float32)
+    b = r.standard_normal(N).astype(np.float32)
+    y = torch.empty((M, N), dtype=out_dtype, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t2va.w8a8_linear(_dev_codes(xq, torch.bfloat16), torch.from_numpy(sx).cuda(), _dev_codes(wq, torch.bfloat16),
+                     torch.from_numpy(sw).cuda(), y, torch.from_numpy(b).cuda(), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    rows = np.array([t * 128 + o for t in range(M // 128) for o in (0, 1, 45, 70, 127)])
+    acc, _ = W8.w8a8_linear(xq[rows], sx[rows], wq, sw, b)
+    _check_linear(y.float().cpu().numpy()[rows], acc, sx[rows], sw, b, out_dtype)
+
+
 @pytest.mark.parametrize("code", CODES, ids=["int8", "bf16codes"])
 def test_w8a8_integer_sum_exact(code):
     """Unit scales, no bias, float32 output: y is the integer sum itself while |sum| < 2^24,
