@@ -251,8 +251,19 @@ def test_bounded_wait_runs_out_and_context_survives():
     t2va.w8a8_linear(_dev_codes(xq, torch.bfloat16), one(M), _dev_codes(wq, torch.bfloat16), one(N), y, status=st)
     torch.cuda.synchronize()
     assert torch.all(y == -1.0)                      # skipped: the word still holds the timeout
+    yw = torch.full((M, 2 * N), -1.0, device="cuda")  # N = 256: the wide kernel skips as well
+    wq2 = np.concatenate([wq, wq])
+    t2va.w8a8_linear(_dev_codes(xq, torch.bfloat16), one(M), _dev_codes(wq2, torch.bfloat16), one(2 * N), yw,
+                     status=st)
+    torch.cuda.synchronize()
+    assert torch.all(yw == -1.0)
     st.zero_()
     t2va.w8a8_linear(_dev_codes(xq, torch.bfloat16), one(M), _dev_codes(wq, torch.bfloat16), one(N), y, status=st)
     torch.cuda.synchronize()
     assert st.item() == 0
     assert np.array_equal(y.cpu().numpy().astype(np.int64), W8.int_dot(xq, wq))
+    t2va.w8a8_linear(_dev_codes(xq, torch.bfloat16), one(M), _dev_codes(wq2, torch.bfloat16), one(2 * N), yw,
+                     status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(yw.cpu().numpy().astype(np.int64), W8.int_dot(xq, wq2))
