@@ -337,14 +337,14 @@ int gemm_tile_n() { return kBN; }
 int gemm_tile_k() { return kBK; }
 
 cudaError_t launch_w8a8_gemm(const GemmArgs& a, bool bf16_out, cudaStream_t st) {
-  static bool attr_done = false;
-  if (!attr_done) {
+  // once per process (a function-local static is initialised exactly once, thread-safely)
+  static const cudaError_t smem_attr = [] {
     cudaError_t e = cudaFuncSetAttribute(k_w8a8_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k_w8a8_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+    return e;
+  }();
+  if (smem_attr != cudaSuccess) return smem_attr;
   const dim3 grid((unsigned)(a.N / kBN), (unsigned)(a.M / kBM));
   if (bf16_out) return launch_pdl_args(k_w8a8_gemm<true>, grid, kGThreads, kGemmSmem, st, a);
   return launch_pdl_args(k_w8a8_gemm<false>, grid, kGThreads, kGemmSmem, st, a);

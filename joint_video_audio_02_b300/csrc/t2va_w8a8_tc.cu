@@ -534,19 +534,18 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// The driver's tensor-map encoder, looked up once per process (a function-local static is
+// initialised exactly once, thread-safely); null if the driver does not offer it.
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static const EncodeTiledFn fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-    else
-      cudaGetLastError();
-  }
+      return reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+    return static_cast<EncodeTiledFn>(nullptr);
+  }();
   return fn;
 }
 
@@ -593,19 +592,25 @@ cudaError_t launch_w8a8_tc_selftest(int* status, cudaStream_t st) {
 // at most one per tile.
 static cudaError_t launch_w8a8_tc_wide(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a, bool bf16_out,
                                 cudaStream_t st) {
-  static bool attr_done = false;
-  static int sms = 0;
-  if (!attr_done) {
+  // once per process, on the device current at the first call (one device per process)
+  struct Setup {
+    cudaError_t e;
+    int sms;
+  };
+  static const Setup setup = [] {
+    Setup r = {cudaSuccess, 0};
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_w8a8_tc_wide<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_w8a8_tc_wide<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+    r.e = cudaGetDevice(&dev);
+    if (r.e == cudaSuccess) r.e = cudaDeviceGetAttribute(&r.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (r.e == cudaSuccess)
+      r.e = cudaFuncSetAttribute(k_w8a8_tc_wide<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWSmem);
+    if (r.e == cudaSuccess)
+      r.e = cudaFuncSetAttribute(k_w8a8_tc_wide<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWSmem);
+    if (r.e == cudaSuccess && r.sms <= 0) r.e = cudaErrorInvalidValue;
+    return r;
+  }();
+  if (setup.e != cudaSuccess) return setup.e;
+  const int sms = setup.sms;
   const int64_t ntiles = (a.M / kTM) * (a.N / kWN);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(ntiles < sms ? ntiles : sms));
@@ -625,14 +630,13 @@ cudaError_t launch_w8a8_tc(const GemmArgs& a, bool bf16_out, cudaStream_t st) {
   CUtensorMap ma, mb;
   if (!make_map(&ma, a.xq, a.M, a.K) || !make_map(&mb, a.wq, a.N, a.K)) return cudaErrorInvalidValue;
   if (a.N % kWN == 0 && !a.selftest_wait) return launch_w8a8_tc_wide(ma, mb, a, bf16_out, st);
-  static bool attr_done = false;
-  if (!attr_done) {
+  static const cudaError_t smem_attr = [] {
     cudaError_t e = cudaFuncSetAttribute(k_w8a8_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k_w8a8_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+    return e;
+  }();
+  if (smem_attr != cudaSuccess) return smem_attr;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(a.N / kTN), (unsigned)(a.M / kTM));
   cfg.blockDim = dim3(kTThreads);
