@@ -133,6 +133,41 @@ def test_residual_modnorm_general_gate():
     assert np.all(np.abs(y - ref_y) <= bound)
 
 
+def test_residual_modnorm_bench_size_sampled():
+    """The benchmark's launch: 28,672 token rows x 4096 (the 1024x1792 video tokens), bf16,
+    one sample's gate in [0, 1), scale and shift, h' stored. Rows sampled across the grid:
+    h' within one unit of the exactly rounded value, y within the bound of the
+    normalisation of the oracle's h' plus the effect of that unit."""
+    rows, D = 28672, 4096
+    r = np.random.default_rng(5)
+    th = torch.from_numpy(r.standard_normal((rows, D), dtype=np.float32)).to(torch.bfloat16)
+    tu = torch.from_numpy(r.standard_normal((rows, D), dtype=np.float32)).to(torch.bfloat16)
+    gate = r.uniform(0, 1, (1, D)).astype(np.float32)
+    scale = (r.uniform(0, 1, (1, D)) - 0.5).astype(np.float32)
+    shift = (r.uniform(0, 1, (1, D)) - 0.5).astype(np.float32)
+    h, u = th.cuda(), tu.cuda()
+    y, h_out = torch.empty_like(h), torch.empty_like(h)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    t2va.residual_modnorm(h, y, u=u, gate=dev(gate), scale=dev(scale), shift=dev(shift), eps=1e-6, h_out=h_out)
+    torch.cuda.synchronize()
+    rs = np.unique(np.concatenate([np.arange(0, rows, 487), [1, rows - 2, rows - 1]]))
+    ri = torch.from_numpy(rs).cuda()
+    got_h = h_out[ri].float().cpu().numpy().astype(np.float64)
+    got_y = y[ri].float().cpu().numpy().astype(np.float64)
+    n = len(rs)
+    ref_h2, ref_y = F.residual_modnorm(th[rs].float().numpy(), tu[rs].float().numpy(), gate, scale, shift, 1e-6, n,
+                                       _round(torch.bfloat16))
+    diff = np.abs(got_h - ref_h2)
+    assert np.all(diff <= _ulp(ref_h2, torch.bfloat16) + 1e-30)
+    assert (diff > 0).mean() < 1e-2
+    ms = np.mean(ref_h2 * ref_h2, axis=1, keepdims=True)
+    rr = 1.0 / np.sqrt(ms + 1e-6)
+    sc, sh = F.per_row(scale, n, n), F.per_row(shift, n, n)
+    mag = np.abs(ref_h2 * rr * (1 + sc)) + np.abs(sh)
+    bound = 2 * _ulp(ref_y, torch.bfloat16) + 1e-5 * mag + diff * rr * np.abs(1 + sc)
+    assert np.all(np.abs(got_y - ref_y) <= bound)
+
+
 def test_residual_modnorm_errors():
     h = torch.zeros((4, 128), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(t2va.T2VAError) as e:

@@ -225,6 +225,36 @@ def test_w8a8_forward_matches_oracle(code):
     _check_linear(y.float().cpu().numpy(), acc, ref_sx, sw, b, torch.bfloat16)
 
 
+def test_w8a8_bench_size_sampled():
+    """The operator at the benchmark's size and launch: x [28672, 4096] bf16 (the
+    1024x1792 video tokens) quantised per row on the device to bf16 codes, weights
+    [4096, 4096] quantised once by the oracle, bias, bf16 out, through the persistent
+    128 x 256 tensor-core kernel. Rows sampled from every other row tile, in every TMEM
+    lane quadrant: their codes and scales bit for bit, their outputs within the bound of
+    the oracle's exact sums."""
+    M, N, K = 28672, 4096, 4096
+    r = np.random.default_rng(31)
+    tx = torch.from_numpy(r.standard_normal((M, K), dtype=np.float32)).to(torch.bfloat16)
+    w = r.standard_normal((N, K), dtype=np.float32) * 0.02
+    wq, sw = W8.quantize_rows(w)
+    b = (r.standard_normal(N) * 0.1).astype(np.float32)
+    q = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    sx = torch.empty(M, device="cuda")
+    t2va.quantize_rows(tx.cuda(), q, sx)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t2va.w8a8_linear(q, sx, _dev_codes(wq, torch.bfloat16), torch.from_numpy(sw).cuda(), y,
+                     torch.from_numpy(b).cuda(), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    rows = np.array([t * 128 + (37 * t) % 128 for t in range(0, M // 128, 2)])
+    ref_xq, ref_sx, acc, _ = W8.w8a8_forward(tx[rows].float().numpy(), wq, sw, b)
+    ri = torch.from_numpy(rows).cuda()
+    assert np.array_equal(q[ri].float().cpu().numpy().astype(np.int64), ref_xq.astype(np.int64))
+    assert np.array_equal(sx[ri].cpu().numpy(), ref_sx)
+    _check_linear(y[ri].float().cpu().numpy(), acc, ref_sx, sw, b, torch.bfloat16)
+
+
 def test_w8a8_guard():
     z = torch.zeros((100, 128), dtype=torch.int8, device="cuda")
     with pytest.raises(t2va.T2VAError) as e:
