@@ -129,7 +129,8 @@ def _dev_codes(q, code):
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("M,N,K,bias", [(128, 128, 128, True), (256, 384, 512, False),
                                         (384, 256, 4096, True), (128, 640, 1152, True),
-                                        (256, 128, 8192, False)])
+                                        (256, 128, 8192, False), (128, 256, 8192, True),
+                                        (256, 512, 2048, False)])
 def test_w8a8_linear_parity(code, out_dtype, M, N, K, bias):
     xq = _codes(M + K, M, K, extreme=True)
     wq = _codes(N + K + 1, N, K, extreme=True)
