@@ -93,7 +93,8 @@ enum {
 /* A bounded pipeline wait of the tensor-core W8A8 kernel ran out (its output is
  * incomplete). No objective kernel waits on another CTA, so the objective never sets it. */
 #define T2VA_STATUS_TIMEOUT 0x2
-/* Reserved (no kernel checks the workspace, so it is never set). */
+/* Never set: no kernel reads the workspace header (the bit keeps its value for ABI
+ * compatibility). */
 #define T2VA_STATUS_BAD_WORKSPACE 0x4
 
 /* Static description of a return code (never NULL). */
@@ -114,8 +115,8 @@ size_t t2va_workspace_bytes(int batch, int num_modalities);
 
 /* Zero a workspace (16-byte aligned device memory of `workspace_bytes`) on
  * `stream` and write its header. Optional: the objective entry points do not
- * depend on the workspace's contents. `timeout_ms` is recorded in the header
- * for compatibility and not used. */
+ * depend on the workspace's contents. `timeout_ms` is ignored (kept for ABI
+ * compatibility). */
 int t2va_workspace_init(void* workspace, size_t workspace_bytes, uint32_t timeout_ms,
                         cudaStream_t stream);
 
@@ -312,8 +313,8 @@ int t2va_residual_modnorm(int64_t rows, int64_t D, int64_t rows_per_sample, t2va
 int t2va_selftest_wait_timeout(int* status, cudaStream_t stream);
 
 /* Bytes of the library's own scratch array used by
- * t2va_stage3_objective_noalloc (1 MiB). Every GPU that loads the library holds
- * this much device memory until the process exits. */
+ * t2va_stage3_objective_noalloc (1 MiB). Every GPU on which the library's module
+ * is loaded holds this much device memory until the process exits. */
 #define T2VA_NOALLOC_SCRATCH_BYTES (1u << 20)
 
 /* The stage-3 objective without a caller-provided workspace.
@@ -331,13 +332,18 @@ int t2va_selftest_wait_timeout(int* status, cudaStream_t stream);
  * device memory per GPU. The call allocates nothing: no cudaMalloc, no cudaFree
  * and no allocating library routine.
  *
- * - Limit: the workspace that `batch` and `num_modalities` need
- *   (t2va_workspace_bytes: 16 KiB per sample and modality) must fit in the
- *   scratch, so at most 31 samples of 2 modalities per call. A larger batch
- *   returns T2VA_ERROR_WORKSPACE, and nothing is enqueued.
+ * - Limit: the partial sums of the call (16 KiB per sample and modality, the
+ *   workspace that t2va_workspace_bytes counts without its 256-byte header) must
+ *   fit in the scratch, so at most 32 samples of 2 modalities per call. A larger
+ *   batch returns T2VA_ERROR_WORKSPACE, and nothing is enqueued.
  * - First call: the first call on each device, with that device current, looks
- *   up the scratch's device address (cudaGetSymbolAddress) and keeps it. Make
- *   that first call before any stream capture on that device.
+ *   up the scratch's device address (cudaGetSymbolAddress) and keeps it. Under
+ *   CUDA's lazy module loading that lookup is also what loads the library's module
+ *   and its 1 MiB array onto the device, so the first call can fail with
+ *   T2VA_ERROR_CUDA when device memory is exhausted: make it during set-up, before
+ *   the host's allocator takes the memory and before any stream capture on that
+ *   device. A device reset (cudaDeviceReset) unloads the module and invalidates
+ *   the kept address: do not call this entry point again after one.
  * - Sharing: every call on a device shares the one scratch array. A call's first
  *   kernel writes the partial sums its second kernel reads, so the array needs no
  *   clearing, but calls that overlap on the GPU (on different streams or from

@@ -1,6 +1,6 @@
 // C-ABI entry points of the joint video-audio distillation objective library.
 // Argument checking, device queries and launch planning; the arithmetic lives
-// in t2va_noise.cu and t2va_objective.cu. Declarations and the contract of
+// in t2va_noise.cu, t2va_objective.cu and the W8A8 and fused normalisation files. Declarations and the contract of
 // every entry point are in include/t2va.h.
 #include <cmath>
 #include <cstdint>
@@ -98,16 +98,24 @@ int check_scalar_out(const void* p, bool required) {
     if (rc_ != T2VA_SUCCESS) return rc_; \
   } while (0)
 
-// Shared tail of the three objective entry points.
-int run_objective(ObjectiveArgs& a, t2va_dtype dt, int mode, void* workspace, size_t ws_size,
+// The workspace as the objective sees it, from a caller's pointer and size: a null body
+// when the pointer is null or misaligned or the size holds no header (the call then
+// fails the workspace check after every argument check).
+WsRef caller_workspace(void* workspace, size_t bytes) {
+  WsRef w{nullptr, 0};
+  if (workspace == nullptr || !aligned(workspace, 16) || bytes < kWsHeaderBytes) return w;
+  w.body = reinterpret_cast<unsigned char*>(workspace) + kWsHeaderBytes;
+  w.body_bytes = bytes - kWsHeaderBytes;
+  return w;
+}
+
+// Shared tail of the objective entry points: the workspace check, the plan, the launch.
+int run_objective(ObjectiveArgs& a, t2va_dtype dt, int mode, const WsRef& ws,
                   cudaStream_t stream) {
   DeviceInfo dev;
   if (!current_device(&dev)) return T2VA_ERROR_CUDA;
-  const size_t need = ws_bytes(a.B, a.M, dev.sm_count);
-  if (workspace == nullptr || !aligned(workspace, 16) || ws_size < need) return T2VA_ERROR_WORKSPACE;
-  unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
-  a.partials = reinterpret_cast<float*>(ws + kWsHeaderBytes);
-  a.gmax = dev.sm_count;
+  if (ws.body == nullptr || ws.body_bytes < ws_body_bytes(a.B, a.M)) return T2VA_ERROR_WORKSPACE;
+  a.partials = reinterpret_cast<float*>(ws.body);
   for (int m = 0; m < a.M; ++m) {
     const bool s_ok = a.grad_s[m] == nullptr || aligned(a.grad_s[m], 32);
     const bool d_ok = a.grad_d[m] == nullptr || aligned(a.grad_d[m], 32);
@@ -117,8 +125,7 @@ int run_objective(ObjectiveArgs& a, t2va_dtype dt, int mode, void* workspace, si
     if (s_ok && d_ok) a.wide_mask |= 1u << m;
   }
   ObjectiveLaunch l;
-  if (!plan_objective(a, dt, mode, dev.sm_count, dev.smem_optin, dev.l2_bytes, &l))
-    return T2VA_ERROR_CUDA;
+  if (!plan_objective(a, dt, dev.sm_count, &l)) return T2VA_ERROR_CUDA;
   const cudaError_t e = launch_objective(a, dt, mode, l, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -183,20 +190,21 @@ int run_noise(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype
   return T2VA_SUCCESS;
 }
 
+}  // namespace
+
 // The stage-3 entry points: without guidance (x0_teacher_hat_uncond and guidance
 // null), x0_teacher_hat is the teacher prediction; with it, the conditional one.
-int stage3_impl(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
-                const void* const* z_t, const void* const* x0_teacher,
-                const void* const* x0_student, const void* const* x0_student_tangent,
-                const float* t,
-                const void* const* zhat0, const void* const* x0_teacher_hat,
-                const void* const* x0_teacher_hat_uncond, const float* guidance,
-                const void* const* x0_fake,
-                float beta, float gamma, float eps_scm, float eps_dmd,
-                const float* weight, float lambda_scm, float lambda_dmd,
-                float* const* grad_x0_student, float* const* grad_zhat0, int accumulate,
-                float* loss, float* loss_scm, float* loss_dmd, float* norm, float* cdmd,
-                void* workspace, size_t workspace_bytes, int* status, cudaStream_t stream) {
+int t2va::stage3_entry(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+                       const void* const* z_t, const void* const* x0_teacher,
+                       const void* const* x0_student, const void* const* x0_student_tangent,
+                       const float* t, const void* const* zhat0,
+                       const void* const* x0_teacher_hat,
+                       const void* const* x0_teacher_hat_uncond, const float* guidance,
+                       const void* const* x0_fake, float beta, float gamma, float eps_scm,
+                       float eps_dmd, const float* weight, float lambda_scm, float lambda_dmd,
+                       float* const* grad_x0_student, float* const* grad_zhat0, int accumulate,
+                       float* loss, float* loss_scm, float* loss_dmd, float* norm, float* cdmd,
+                       const WsRef& ws, int* status, cudaStream_t stream) {
   const int M = num_modalities;
   T2VA_TRY(check_geometry(batch, M, seg));
   T2VA_TRY(check_dtype(dtype));
@@ -254,11 +262,8 @@ int stage3_impl(int batch, int num_modalities, const t2va_segment* seg, t2va_dty
   a.norm = norm;
   a.cdmd = cdmd;
   a.status = status;
-  return run_objective(a, dtype, cfg ? (kModeStage3 | kModeCfg) : kModeStage3, workspace,
-                      workspace_bytes, stream);
+  return run_objective(a, dtype, cfg ? (kModeStage3 | kModeCfg) : kModeStage3, ws, stream);
 }
-
-}  // namespace
 
 extern "C" {
 
@@ -280,7 +285,7 @@ size_t t2va_workspace_bytes(int batch, int num_modalities) {
   if (batch < 0 || num_modalities < 1 || num_modalities > kMaxM) return 0;
   DeviceInfo dev;
   if (!current_device(&dev)) return 0;
-  return ws_bytes(batch, num_modalities, dev.sm_count);
+  return ws_bytes(batch, num_modalities);
 }
 
 int t2va_quantize_rows(int64_t rows, int64_t cols, t2va_dtype dtype, const void* x, int64_t ld_x,
@@ -404,14 +409,11 @@ int t2va_selftest_wait_timeout(int* status, cudaStream_t stream) {
   return T2VA_SUCCESS;
 }
 
-int t2va_workspace_init(void* workspace, size_t workspace_bytes, uint32_t timeout_ms,
+int t2va_workspace_init(void* workspace, size_t workspace_bytes, uint32_t /*timeout_ms*/,
                         cudaStream_t stream) {
   if (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < kWsHeaderBytes)
     return T2VA_ERROR_WORKSPACE;
-  DeviceInfo dev;
-  if (!current_device(&dev)) return T2VA_ERROR_CUDA;
-  const uint64_t ns = (uint64_t)(timeout_ms ? timeout_ms : 1000u) * 1000000ull;
-  if (launch_workspace_init(workspace, workspace_bytes, ns, (uint32_t)dev.sm_count, stream) != cudaSuccess) {
+  if (launch_workspace_init(workspace, workspace_bytes, stream) != cudaSuccess) {
     cudaGetLastError();
     return T2VA_ERROR_CUDA;
   }
@@ -497,7 +499,7 @@ int t2va_scm_objective(int batch, int num_modalities, const t2va_segment* seg, t
   a.loss = loss;
   a.norm = norm;
   a.status = status;
-  return run_objective(a, dtype, kModeScm, workspace, workspace_bytes, stream);
+  return run_objective(a, dtype, kModeScm, caller_workspace(workspace, workspace_bytes), stream);
 }
 
 int t2va_dmd_objective(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
@@ -533,7 +535,7 @@ int t2va_dmd_objective(int batch, int num_modalities, const t2va_segment* seg, t
   a.loss = loss;
   a.cdmd = cdmd;
   a.status = status;
-  return run_objective(a, dtype, kModeDmd, workspace, workspace_bytes, stream);
+  return run_objective(a, dtype, kModeDmd, caller_workspace(workspace, workspace_bytes), stream);
 }
 
 int t2va_stage3_objective(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
@@ -548,11 +550,11 @@ int t2va_stage3_objective(int batch, int num_modalities, const t2va_segment* seg
                           float* loss, float* loss_scm, float* loss_dmd, float* norm, float* cdmd,
                           void* workspace, size_t workspace_bytes, int* status,
                           cudaStream_t stream) {
-  return stage3_impl(batch, num_modalities, seg, dtype, z_t, x0_teacher, x0_student,
-                     x0_student_tangent, t, zhat0, x0_teacher_hat, nullptr, nullptr, x0_fake, beta,
-                     gamma, eps_scm, eps_dmd, weight, lambda_scm, lambda_dmd, grad_x0_student,
-                     grad_zhat0, accumulate, loss, loss_scm, loss_dmd, norm, cdmd, workspace,
-                     workspace_bytes, status, stream);
+  return stage3_entry(batch, num_modalities, seg, dtype, z_t, x0_teacher, x0_student,
+                      x0_student_tangent, t, zhat0, x0_teacher_hat, nullptr, nullptr, x0_fake, beta,
+                      gamma, eps_scm, eps_dmd, weight, lambda_scm, lambda_dmd, grad_x0_student,
+                      grad_zhat0, accumulate, loss, loss_scm, loss_dmd, norm, cdmd,
+                      caller_workspace(workspace, workspace_bytes), status, stream);
 }
 
 int t2va_stage3_objective_cfg(
@@ -566,11 +568,12 @@ int t2va_stage3_objective_cfg(
     float* loss_scm, float* loss_dmd, float* norm, float* cdmd, void* workspace,
     size_t workspace_bytes, int* status, cudaStream_t stream) {
   if (x0_teacher_hat_uncond == nullptr) return T2VA_ERROR_INVALID_ARGUMENT;
-  return stage3_impl(batch, num_modalities, seg, dtype, z_t, x0_teacher, x0_student,
-                     x0_student_tangent, t, zhat0, x0_teacher_hat_cond, x0_teacher_hat_uncond,
-                     guidance, x0_fake, beta, gamma, eps_scm, eps_dmd, weight, lambda_scm,
-                     lambda_dmd, grad_x0_student, grad_zhat0, accumulate, loss, loss_scm,
-                     loss_dmd, norm, cdmd, workspace, workspace_bytes, status, stream);
+  return stage3_entry(batch, num_modalities, seg, dtype, z_t, x0_teacher, x0_student,
+                      x0_student_tangent, t, zhat0, x0_teacher_hat_cond, x0_teacher_hat_uncond,
+                      guidance, x0_fake, beta, gamma, eps_scm, eps_dmd, weight, lambda_scm,
+                      lambda_dmd, grad_x0_student, grad_zhat0, accumulate, loss, loss_scm,
+                      loss_dmd, norm, cdmd, caller_workspace(workspace, workspace_bytes), status,
+                      stream);
 }
 
 }  // extern "C"

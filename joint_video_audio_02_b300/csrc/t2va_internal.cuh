@@ -16,17 +16,14 @@ constexpr uint32_t kWsMagic = 0x54325641u;  // "T2VA"
 
 // ---------------------------------------------------------------------------
 // Workspace layout (caller-owned device memory)
-//   [0, 256)     header (written by t2va_workspace_init; the kernels do not need it)
+//   [0, 256)     header: written by t2va_workspace_init; no kernel reads it
 //   [256, ...)   partial sums: float4 {sum g_sCM^2, sum |zhat0 - y_T|, sum g_DMD^2, 0}
 //                per (sample, modality, chunk), kMaxChunks chunks per (sample, modality),
 //                written by the first kernel of a call and read by the second
 // ---------------------------------------------------------------------------
 struct WsHeader {
   uint32_t magic;
-  uint32_t reserved0;
-  uint64_t timeout_ns;   // recorded by t2va_workspace_init (no wait in the kernels uses it)
-  uint32_t gmax;
-  uint32_t pad[59];
+  uint32_t pad[63];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
@@ -34,9 +31,14 @@ constexpr size_t kWsHeaderBytes = 256;
 constexpr int kQuantities = 3;  // sum g_sCM^2, sum |zhat0 - y_T|, sum g_DMD^2
 constexpr int kMaxChunks = 1024;  // chunks per (sample, modality) row
 
-inline size_t ws_bytes(int B, int M, int /*sm_count*/) {
-  return kWsHeaderBytes + (size_t)B * M * kMaxChunks * 16;
-}
+inline size_t ws_body_bytes(int B, int M) { return (size_t)B * M * kMaxChunks * 16; }
+inline size_t ws_bytes(int B, int M) { return kWsHeaderBytes + ws_body_bytes(B, M); }
+
+// A workspace as the objective sees it: the partial-sum area behind the header.
+struct WsRef {
+  unsigned char* body;
+  size_t body_bytes;
+};
 
 // Modes of the objective kernel.
 enum : int { kModeScm = 1, kModeDmd = 2, kModeStage3 = 3, kModeCfg = 4 };
@@ -67,7 +69,6 @@ struct ObjectiveArgs {
   float* norm;
   float* cdmd;
   float* partials;             // float4 [B][M][kMaxChunks]
-  int gmax;
   int* status;
   // launch plan (filled by plan_objective)
   int vpc;                     // 16-byte vectors per chunk (a multiple of one CTA's batch)
@@ -105,12 +106,24 @@ struct ObjectiveLaunch {
 };
 // Chooses the chunks and the grid for `a` (fills the plan fields); returns false if
 // the problem is too large for the workspace layout.
-bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int mode, int sm_count, size_t smem_optin,
-                    size_t l2_bytes, ObjectiveLaunch* out);
+bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int sm_count, ObjectiveLaunch* out);
 cudaError_t launch_objective(const ObjectiveArgs& a, t2va_dtype dt, int mode,
                              const ObjectiveLaunch& l, cudaStream_t st);
-cudaError_t launch_workspace_init(void* ws, size_t bytes, uint64_t timeout_ns, uint32_t gmax,
-                                  cudaStream_t st);
+cudaError_t launch_workspace_init(void* ws, size_t bytes, cudaStream_t st);
+
+// The stage-3 entry points after their own checks (t2va_api.cu): argument validation,
+// then the workspace check, then the launch. Without guidance x0_teacher_hat_uncond
+// and guidance are null. A workspace whose body is null fails the workspace check.
+int stage3_entry(int batch, int num_modalities, const t2va_segment* seg, t2va_dtype dtype,
+                 const void* const* z_t, const void* const* x0_teacher,
+                 const void* const* x0_student, const void* const* x0_student_tangent,
+                 const float* t, const void* const* zhat0, const void* const* x0_teacher_hat,
+                 const void* const* x0_teacher_hat_uncond, const float* guidance,
+                 const void* const* x0_fake, float beta, float gamma, float eps_scm,
+                 float eps_dmd, const float* weight, float lambda_scm, float lambda_dmd,
+                 float* const* grad_x0_student, float* const* grad_zhat0, int accumulate,
+                 float* loss, float* loss_scm, float* loss_dmd, float* norm, float* cdmd,
+                 const WsRef& ws, int* status, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Device helpers
@@ -130,28 +143,6 @@ __device__ __forceinline__ void st_stream16(void* p, float4 v) {
   asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
                "f"(v.w)
                : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 // bfloat16 pair (low half = element 0) -> two floats, exact.

@@ -13,7 +13,9 @@
 // Host code cannot use the array's name as a device address: on the host it
 // names a host-side stand-in. So the first call on each device, with that
 // device current, asks the runtime for the array's device address
-// (cudaGetSymbolAddress) and keeps it; later calls on that device reuse it.
+// (cudaGetSymbolAddress) and keeps it; later calls on that device reuse it. A
+// device reset (cudaDeviceReset) unloads the module and invalidates that address:
+// a process that resets a device must not call this entry point afterwards.
 #include <mutex>
 
 #include "t2va_internal.cuh"
@@ -62,27 +64,19 @@ extern "C" int t2va_stage3_objective_noalloc(
     float* const* grad_x0_student, float* const* grad_zhat0, int accumulate, float* loss,
     float* loss_scm, float* loss_dmd, float* norm, float* cdmd, int* status,
     cudaStream_t stream) {
-  // Every argument check of t2va_stage3_objective comes before its workspace
-  // check, so a call without a workspace returns T2VA_ERROR_WORKSPACE exactly when
-  // everything else is valid, and enqueues nothing. An empty batch returns success.
-  const int pre = t2va_stage3_objective(
-      batch, num_modalities, seg, dtype, z_t, x0_teacher, x0_student, x0_student_tangent, t,
-      zhat0, x0_teacher_hat, x0_fake, beta, gamma, eps_scm, eps_dmd, weight, lambda_scm,
-      lambda_dmd, grad_x0_student, grad_zhat0, accumulate, loss, loss_scm, loss_dmd, norm, cdmd,
-      nullptr, 0, status, stream);
-  if (pre != T2VA_ERROR_WORKSPACE) return pre;
-  // the scratch must hold the workspace this batch needs on this device
-  const size_t need = t2va_workspace_bytes(batch, num_modalities);
-  if (need == 0) return T2VA_ERROR_CUDA;
-  if (need > (size_t)T2VA_NOALLOC_SCRATCH_BYTES) return T2VA_ERROR_WORKSPACE;
-  void* ws = nullptr;
-  const int rc = scratch_address(&ws);
+  void* scratch = nullptr;
+  const int rc = scratch_address(&scratch);
   if (rc != T2VA_SUCCESS) return rc;
-  // The array keeps whatever the last call left there; that is harmless, because the
-  // call's first kernel writes every partial sum its second kernel reads.
-  return t2va_stage3_objective(batch, num_modalities, seg, dtype, z_t, x0_teacher, x0_student,
-                               x0_student_tangent, t, zhat0, x0_teacher_hat, x0_fake, beta, gamma,
-                               eps_scm, eps_dmd, weight, lambda_scm, lambda_dmd, grad_x0_student,
-                               grad_zhat0, accumulate, loss, loss_scm, loss_dmd, norm, cdmd, ws,
-                               (size_t)T2VA_NOALLOC_SCRATCH_BYTES, status, stream);
+  // the scratch is the workspace's partial-sum area (no header is needed)
+  const WsRef ws{reinterpret_cast<unsigned char*>(scratch), (size_t)T2VA_NOALLOC_SCRATCH_BYTES};
+  // The same checks, in the same order, as t2va_stage3_objective: every argument check,
+  // then the scratch must hold what this batch needs (else T2VA_ERROR_WORKSPACE), and
+  // nothing is enqueued on an error. The scratch keeps what the last call left there;
+  // that is harmless, because the call's first kernel writes every partial sum its
+  // second kernel reads.
+  return stage3_entry(batch, num_modalities, seg, dtype, z_t, x0_teacher, x0_student,
+                      x0_student_tangent, t, zhat0, x0_teacher_hat, nullptr, nullptr, x0_fake,
+                      beta, gamma, eps_scm, eps_dmd, weight, lambda_scm, lambda_dmd,
+                      grad_x0_student, grad_zhat0, accumulate, loss, loss_scm, loss_dmd, norm,
+                      cdmd, ws, status, stream);
 }

@@ -552,25 +552,18 @@ cudaError_t launch_t(const ObjectiveArgs& a, const ObjectiveLaunch& l, cudaStrea
   return launch_pdl(k_grads<T, MODE>, l.grid, st, a);
 }
 
-__global__ void k_ws_init(uint4* ws, size_t n16, uint64_t timeout_ns, uint32_t gmax) {
+__global__ void k_ws_init(uint4* ws, size_t n16) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16;
        i += (size_t)gridDim.x * blockDim.x)
     ws[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    // block 0 zeroed the header above; write its fields after that block's barrier
-    WsHeader* h = reinterpret_cast<WsHeader*>(ws);
-    h->timeout_ns = timeout_ns;
-    h->gmax = gmax;
-    __threadfence();
-    h->magic = kWsMagic;
-  }
+  // block 0 zeroed the header above; write its magic after that block's barrier
+  if (blockIdx.x == 0 && threadIdx.x == 0) reinterpret_cast<WsHeader*>(ws)->magic = kWsMagic;
 }
 
 }  // namespace
 
-bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int /*mode*/, int sm_count,
-                    size_t /*smem_optin*/, size_t /*l2_bytes*/, ObjectiveLaunch* out) {
+bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int sm_count, ObjectiveLaunch* out) {
   const int VE = dt == T2VA_BFLOAT16 ? 8 : 4;
   int64_t nvec_max = 0, grid1 = 0, total = 0;
   for (int m = 0; m < a.M; ++m) {
@@ -637,11 +630,10 @@ cudaError_t launch_objective(const ObjectiveArgs& a, t2va_dtype dt, int mode,
   return launch_t<float, kModeStage3>(a, l, st);
 }
 
-cudaError_t launch_workspace_init(void* ws, size_t bytes, uint64_t timeout_ns, uint32_t gmax,
-                                  cudaStream_t st) {
+cudaError_t launch_workspace_init(void* ws, size_t bytes, cudaStream_t st) {
   const size_t n16 = bytes / 16;
   int blocks = (int)std::min<size_t>(1024, std::max<size_t>(1, (n16 + 255) / 256));
-  k_ws_init<<<blocks, 256, 0, st>>>(reinterpret_cast<uint4*>(ws), n16, timeout_ns, gmax);
+  k_ws_init<<<blocks, 256, 0, st>>>(reinterpret_cast<uint4*>(ws), n16);
   return cudaGetLastError();
 }
 

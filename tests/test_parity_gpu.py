@@ -118,20 +118,45 @@ def test_dmd_parity():
     compare(gpu, ref, wl.dtype, S.DMD)
 
 
-def test_stage3_two_large_samples_one_slot():
-    """Two 1024x1792 samples: their directions do not fit on chip together, so the
-    kernel runs with one shared-memory slot."""
+def test_stage3_two_1024x1792_samples():
+    """Two 1024x1792 samples (7.4M elements, 922K vectors): 1800 chunks of one
+    512-vector batch, about four waves of three CTAs per SM, and inputs (103 MB) that
+    nearly fill L2 between the two passes."""
     inp = S.make_inputs(2, S.workload("stage3_1024x1792_bf16").numels, "bf16", S.STAGE3, seed=(103,))
     p = Params()
     compare(gpu_run(inp, p, S.STAGE3), oracle_run(inp, p, S.STAGE3), "bf16", S.STAGE3)
 
 
-def test_stage3_recompute_beyond_shared_memory():
-    """A 12M-element sample: part of each CTA's slice does not fit in shared memory and
-    is recomputed from the inputs in the write phase."""
+def test_stage3_one_12M_element_row():
+    """One sample whose video row has 12M elements (1.5M vectors): the row needs more
+    than the 1024 chunks a row may have at one batch per chunk, so its chunks hold
+    three 512-vector batches (977 chunks); the call's inputs (168 MB) do not fit in
+    L2, so the gradient pass reads them from HBM again."""
     inp = S.make_inputs(1, [12_000_000, 1000], "bf16", S.STAGE3, seed=(104,))
     p = Params(weight=(1.0, 2.0))
     compare(gpu_run(inp, p, S.STAGE3), oracle_run(inp, p, S.STAGE3), "bf16", S.STAGE3)
+
+
+# the configs clamp t to [1e-3, pi/2 - 1e-3]; both ends, in float32 as the kernels get them
+T_CLAMP = np.array([1e-3, math.pi / 2 - 1e-3], dtype=np.float32)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("mode", [S.SCM, S.STAGE3])
+@pytest.mark.parametrize("gamma", [0.0, 0.5, 0.9, 1.0])
+@pytest.mark.parametrize("beta", [0.8, 1.0, 1.2])
+def test_clamp_boundary_timesteps(dtype, mode, gamma, beta):
+    """One sample at t = 1e-3 and one at t = pi/2 - 1e-3. There the sCM direction's
+    beta cos t / sqrt(1 - gamma^2 sin^2 t) term nearly cancels the c^2 term of J
+    (t -> 0, beta = 1), the gradient's 1/sin t is 1000, and with gamma = 1 the square
+    root itself shrinks to cos t = 1e-3: the float32 per-sample coefficients must stay
+    within the stated tolerances of the float64 oracle at both ends."""
+    inp = S.make_inputs(2, [20000, 333], dtype, S.STAGE3, seed=(310, int(gamma * 10), int(beta * 10)))
+    p = Params(gamma=gamma, beta=beta)
+    gpu = gpu_run(inp, p, mode, t_override=T_CLAMP)
+    ref = oracle_run(inp, p, mode, t_override=T_CLAMP)
+    assert gpu["status"] == 0
+    compare(gpu, ref, dtype, mode)
 
 
 # --------------------------------------------------------------------------
@@ -307,11 +332,15 @@ def test_workspace_contents_do_not_matter():
     for k in ("grad_x0_student", "grad_zhat0"):
         for x, y in zip(clean[k], dirty[k]):
             assert np.array_equal(x, y)
-    # the same workspace for a call with other sizes, then this call again
-    other = S.make_inputs(2, [777, 33], "bf16", S.STAGE3, seed=(401,))
-    gpu_run(other, p, S.STAGE3, workspace=ws)
+    # the same workspace for calls with other sizes, then this call again
+    gpu_run(S.make_inputs(2, [777, 33], "bf16", S.STAGE3, seed=(401,)), p, S.STAGE3, workspace=ws)
+    gpu_run(S.make_inputs(1, [9, 8191], "f32", S.STAGE3, seed=(402,)), p, S.SCM, workspace=ws)
     again = gpu_run(inp, p, S.STAGE3, workspace=ws)
-    assert np.array_equal(clean["loss"], again["loss"])
+    for k in ("loss", "loss_scm", "loss_dmd", "norm", "cdmd"):
+        assert np.array_equal(clean[k], again[k]), k
+    for k in ("grad_x0_student", "grad_zhat0"):
+        for x, y in zip(clean[k], again[k]):
+            assert np.array_equal(x, y)
 
 
 def test_host_errors_on_device():
