@@ -265,6 +265,78 @@ class ClockSampler:
 # GPU arm
 # ---------------------------------------------------------------------------
 
+EXTRA_SHAPES = ["stage3_1024x1792_bf16", "stage3_sweep_b1_bf16", "stage3_sweep_b4_bf16",
+                "stage3_sweep_b16_bf16", "stage3_sweep_b32_bf16"]
+
+
+def objective_rooflines(names, dev, cap_stream, n_launch, l2, peak):
+    """The objective alone at other shapes, timed as the roofline kernel is: a CUDA graph
+    of `n_launch` back-to-back calls over input sets that together exceed 3x L2, replayed
+    once untimed and then timed with CUDA events on the launching stream. The inputs
+    are drawn on the device (N(0, 1), t uniform in [0.05, 1.45]): the kernels' work does
+    not depend on the values."""
+    import torch
+
+    import joint_video_audio_02_b300 as t2va
+
+    out = {}
+    for name in names:
+        w = S.workload(name)
+        tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        n_el = w.batch * sum(w.numels)
+        nbytes = n_el * bytes_per_element("stage3", w.dtype)
+        R = max(2, math.ceil(3 * l2 / (nbytes + 2 * n_el * elem_size(w.dtype))))
+        g = torch.Generator(device=dev)
+        g.manual_seed(1234)
+        sets = []
+        for _ in range(R):
+            d = {f: [torch.randn(w.batch, n, device=dev, generator=g).to(tdt) for n in w.numels]
+                 for f in ("zt", "xT", "xS", "tan", "zh", "yT", "yF")}
+            d["gS"] = [torch.empty(w.batch, n, device=dev) for n in w.numels]
+            d["gD"] = [torch.empty(w.batch, n, device=dev) for n in w.numels]
+            d["t"] = torch.rand(w.batch, device=dev, generator=g) * 1.4 + 0.05
+            d["loss"] = torch.empty(w.batch, device=dev)
+            sets.append(d)
+        ws = t2va.new_workspace(w.batch, w.num_modalities)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def call(d):
+            t2va.stage3_objective(d["zt"], d["xT"], d["xS"], d["tan"], d["t"], d["zh"], d["yT"], d["yF"],
+                                  beta=w.beta, gamma=w.gamma, eps_scm=w.eps_scm, eps_dmd=w.eps_dmd,
+                                  weight=w.weight, lambda_scm=w.lambda_scm, lambda_dmd=w.lambda_dmd,
+                                  grad_x0_student=d["gS"], grad_zhat0=d["gD"], loss=d["loss"],
+                                  workspace=ws, status=st, stream=cap_stream)
+
+        with torch.cuda.stream(cap_stream):
+            for d in sets:
+                call(d)
+        cap_stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap_stream):
+            with torch.cuda.graph(graph, stream=cap_stream):
+                for i in range(n_launch):
+                    call(sets[i % R])
+        reps = max(1, min(10, 2000 // n_launch))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(cap_stream):
+            graph.replay()
+            e0.record(cap_stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(cap_stream)
+        cap_stream.synchronize()
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())} at {name}")
+        us = e0.elapsed_time(e1) * 1e3 / (reps * n_launch)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {"elements": n_el, "algorithmic_bytes_per_launch": nbytes, "mean_launch_us": round(us, 3),
+                     "achieved": round(gbs, 2), "unit": "GB/s", "frac": round(gbs / peak, 4),
+                     "launches_timed": reps * n_launch, "input_sets": R}
+        del graph, sets, ws
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     import torch
 
@@ -405,25 +477,23 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     g_main = capture(S_steps)
     reps, rem = divmod(K, S_steps)
     g_rem = capture(rem, offset=S_steps) if rem else None
-    g_warm = capture(W) if W > 0 else None
+    g_warm = capture(max(W, 3))
     # the dominant kernel alone: back-to-back objective launches over the same rotating sets
     g_obj = capture(S_steps, objective_only=True)
     g_noise = capture(S_steps, noise_only=True)
     torch.cuda.synchronize()
 
+    # The clock sampler runs from before the clock ramp to after the per-kernel legs, so
+    # that even a short timed region lies inside a window with samples.
+    sampler = ClockSampler("GPU-" + str(props.uuid))
+    sampler.start()
     # clock ramp (the GPU leaves its idle clocks only under sustained load), then W warm-up steps
     ramp_t0 = time.time()
     with torch.cuda.stream(cap_stream):
         while time.time() - ramp_t0 < args.clock_ramp_seconds:
             g_main.replay()
             cap_stream.synchronize()
-        if g_warm is not None:
-            g_warm.replay()
     cap_stream.synchronize()
-
-    sampler = ClockSampler("GPU-" + str(props.uuid))
-    sampler.start()
-    time.sleep(0.05)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -431,6 +501,10 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     t_end = torch.cuda.Event(enable_timing=True)
     h0 = time.time()
     with torch.cuda.stream(cap_stream):
+        # The W warm-up steps are replayed, not waited for, right before the start
+        # event: the GPU is busy with them while the host submits the timed graphs, so
+        # no submission latency falls inside the timed region.
+        g_warm.replay()
         t_start.record(cap_stream)
         for _ in range(reps):
             g_main.replay()
@@ -442,8 +516,6 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     h1 = time.time()
     if dist is not None:
         dist.barrier()
-    time.sleep(0.02)
-    sampler.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
     st = int(status.item())
     if st != 0:
@@ -473,16 +545,24 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     noise_mean_ms = o_start.elapsed_time(o_end) / (obj_reps * S_steps)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during the benchmark")
+    peak, peak_kind = measured_peak()
+    extra = None
+    if wl.name == DEFAULT_WORKLOAD and not args.no_extra_shapes:
+        extra = objective_rooflines(EXTRA_SHAPES, dev, cap_stream, min(S_steps, 100), l2, peak)
+    h2 = time.time()
+    time.sleep(0.02)
+    sampler.stop()
 
     elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
     ms_per_step = elapsed_ms / K
     value = whole_job_gbs(world, nb["step"], K, elapsed_ms)
     obj_gbs = nb["objective"] / (obj_mean_ms * 1e-3) / 1e9
-    peak, peak_kind = measured_peak()
-    clocks = sampler.summary(h0, h1)
+    clocks = sampler.summary(ramp_t0, h2)
+    clocks["window"] = ("clock ramp, warm-up, timed steps and the per-kernel legs "
+                        f"({h2 - ramp_t0:.2f} s; timed steps {h1 - h0:.4f} s)")
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(args, wl, host0, sets[:2], status, noise, objective, dev, nb, world, dist)
+    e2e = run_e2e(args, wl, host0, status, noise, objective, dev, nb, world, dist)
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -531,73 +611,115 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
     }
+    if extra is not None:
+        result["objective_at_other_shapes"] = extra
     return result
 
 
-def run_e2e(args, wl, host0, dsets, status, noise, objective, dev, nb, world, dist):
-    """The same steps with host buffers: every step copies its inputs in from pinned host
-    memory and reads its result, the per-sample losses, back to the host (the gradients
-    stay on the device, where the networks' backward pass consumes them). Steps are
-    pipelined the way a data loader feeds a training loop: two device buffer sets
-    alternate, and the copies in, the compute and the copies out run on three streams
-    ordered by events, so step i+1's inputs arrive while step i computes and step i-1's
-    result drains."""
+def _packed(fields_shapes, dev, pinned=False):
+    """One byte block holding every (name, shape, dtype) tensor at a 256-byte aligned
+    offset, and the tensor views into it."""
+    import torch
+    offs, total = [], 0
+    for _, shape, dt in fields_shapes:
+        n = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+        offs.append((total, n))
+        total += (n + 255) // 256 * 256
+    if dev is None:
+        block = torch.empty(total, dtype=torch.uint8, pin_memory=pinned)
+    else:
+        block = torch.empty(total, dtype=torch.uint8, device=dev)
+    views = [block[o:o + n].view(dt).view(shape) for (o, n), (_, shape, dt) in zip(offs, fields_shapes)]
+    return block, views
+
+
+def run_e2e(args, wl, host0, status, noise, objective, dev, nb, world, dist):
+    """The same steps with host buffers, through the public API: every step copies its
+    inputs in from pinned host memory and its results, the float32 gradients and the
+    per-sample losses, back to pinned host memory. Each direction is one copy per step:
+    a step's inputs are packed in one pinned block and land in one device block whose
+    views the library is called with, and the gradients and losses are written into one
+    device block that is read back whole. Steps are pipelined the way a data loader
+    feeds a training loop: two device buffer sets alternate, and the copies in, the
+    compute and the copies out run on three streams ordered by events, so step i+1's
+    inputs arrive while step i computes and step i-1's results drain."""
     import torch
 
     steps = max(4, min(args.steps, args.e2e_steps))
-    fields = input_fields(wl) + ["t"]
-    pinned = {}
-    h2d = 0
-    for f in fields:
-        if f == "t":
-            ts = [torch.from_numpy(host0.t).pin_memory()]
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    M = wl.num_modalities
+    fields = input_fields(wl)
+    in_spec = [(f"{f}{m}", getattr(host0, f)[m].shape, tdt) for f in fields for m in range(M)]
+    in_spec.append(("t", host0.t.shape, torch.float32))
+    hblock, hviews = _packed(in_spec, None, pinned=True)
+    for (name, _, _), v in zip(in_spec, hviews):
+        if name == "t":
+            v.copy_(torch.from_numpy(host0.t))
         else:
-            arrs = getattr(host0, f)
-            if wl.dtype == "bf16":
-                ts = [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for a in arrs]
+            f, m = name[:-1], int(name[-1])
+            a = getattr(host0, f)[m]
+            src = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if wl.dtype == "bf16" else torch.from_numpy(a)
+            v.copy_(src)
+    shapes = [getattr(host0, "z0")[m].shape for m in range(M)]
+    out_spec = [(f"gS{m}", shapes[m], torch.float32) for m in range(M)]
+    if is_stage3(wl):
+        out_spec += [(f"gD{m}", shapes[m], torch.float32) for m in range(M)]
+    out_spec.append(("loss", (wl.batch,), torch.float32))
+    sets = []
+    for _ in range(2):
+        iblock, iviews = _packed(in_spec, dev)
+        oblock, oviews = _packed(out_spec, dev)
+        d = {}
+        for (name, _, _), v in zip(in_spec, iviews):
+            if name == "t":
+                d["t"] = v
             else:
-                ts = [torch.from_numpy(a).pin_memory() for a in arrs]
-        pinned[f] = ts
-        h2d += sum(x.numel() * x.element_size() for x in ts)
-    outs = ["loss"]
-
-    def as_list(v):
-        return v if isinstance(v, list) else [v]
-
-    host_out = [{k: [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in as_list(d[k])]
-                 for k in outs} for d in dsets]
-    d2h = sum(x.numel() * x.element_size() for v in host_out[0].values() for x in v)
+                d.setdefault(name[:-1], []).append(v)
+        for (name, _, _), v in zip(out_spec, oviews):
+            if name == "loss":
+                d["loss"] = v
+            else:
+                d.setdefault(name[:-1], []).append(v)
+        d["zt"] = [torch.empty_like(x) for x in d["z0"]]
+        if is_stage3(wl):
+            d["zht"] = [torch.empty_like(x) for x in d["zhat0"]]
+        if wl.rf_wrapper:
+            d["zrf"] = [torch.empty_like(x) for x in d["z0"]]
+            d["t_rf"] = torch.empty(wl.batch, device=dev)
+            if is_stage3(wl):
+                d["zhrf"] = [torch.empty_like(x) for x in d["zhat0"]]
+        d["norm"] = torch.empty(wl.batch * M, device=dev)
+        d["cdmd"] = torch.empty(wl.batch * M, device=dev)
+        sets.append((iblock, oblock, d))
+    h2d = hblock.numel()
+    host_out = [_packed(out_spec, None, pinned=True)[0] for _ in sets]
+    d2h = host_out[0].numel()
     s_in, s_cmp, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
-    ev_in = [torch.cuda.Event() for _ in dsets]
-    ev_cmp = [torch.cuda.Event() for _ in dsets]
-    ev_out = [torch.cuda.Event() for _ in dsets]
+    ev_in = [torch.cuda.Event() for _ in sets]
+    ev_cmp = [torch.cuda.Event() for _ in sets]
+    ev_out = [torch.cuda.Event() for _ in sets]
 
     def step(i):
-        k = i % len(dsets)
-        d = dsets[k]
+        k = i % len(sets)
+        iblock, oblock, d = sets[k]
         with torch.cuda.stream(s_in):
-            if i >= len(dsets):
+            if i >= len(sets):
                 s_in.wait_event(ev_cmp[k])    # the compute that last read these inputs is done
-            for f in fields:
-                dst = [d["t"]] if f == "t" else d[f]
-                for a, b in zip(dst, pinned[f]):
-                    a.copy_(b, non_blocking=True)
+            iblock.copy_(hblock, non_blocking=True)
             ev_in[k].record(s_in)
         with torch.cuda.stream(s_cmp):
             s_cmp.wait_event(ev_in[k])
-            if i >= len(dsets):
+            if i >= len(sets):
                 s_cmp.wait_event(ev_out[k])   # the copy-out that last read these outputs is done
             noise(d, s_cmp)
             objective(d, s_cmp)
             ev_cmp[k].record(s_cmp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_cmp[k])
-            for key in outs:
-                for a, b in zip(host_out[k][key], as_list(d[key])):
-                    a.copy_(b, non_blocking=True)
+            host_out[k].copy_(oblock, non_blocking=True)
             ev_out[k].record(s_out)
 
-    for i in range(len(dsets)):
+    for i in range(len(sets)):
         step(i)
     torch.cuda.synchronize()
     if dist is not None:
@@ -614,8 +736,10 @@ def run_e2e(args, wl, host0, dsets, status, noise, objective, dev, nb, world, di
     return {"value": round(whole_job_gbs(world, nb["step"], steps, ms), 3), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": ms / steps,
-            "pipeline": "2 device buffer sets; copy-in, compute and copy-out streams",
-            "read_back": "per-sample losses (the gradients stay on the device)"}
+            "link_gbs_per_step": round((h2d + d2h) / (ms / steps * 1e-3) / 1e9, 2),
+            "pipeline": "2 device buffer sets; copy-in, compute and copy-out streams; one "
+                        "pinned-block copy per direction per step",
+            "read_back": "float32 gradients (every modality, both terms) and per-sample losses"}
 
 
 # ---------------------------------------------------------------------------
@@ -669,6 +793,50 @@ def cpu_baseline(wl: S.Workload, budget_s: float) -> dict:
     return {"value": round(nbytes * reps / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"sample 0 of {wl.batch} ({sum(one.numels):,} elements: noising + objective), "
                       f"{reps} passes in {dt:.1f} s; numpy float64, single thread"}
+
+
+def _oracle_worker(job):
+    """One process of the all-core baseline: the oracle on one sample, repeated for
+    about `budget` seconds; returns (algorithmic bytes processed, seconds)."""
+    name, sample, budget = job
+    wl = S.workload(name)
+    one = bounded_sample(wl, 1.0)
+    inp = S.make_workload_inputs(one, seed_offset=sample)
+    nbytes = step_bytes(one)["step"]
+    oracle_pass(one, inp)  # first pass untimed (imports, caches)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_pass(one, inp)
+        reps += 1
+        if time.perf_counter() - t0 >= budget:
+            break
+    return nbytes * reps, time.perf_counter() - t0
+
+
+def cpu_baseline_all_cores(wl: S.Workload, budget_s: float, max_workers: int = 64) -> dict:
+    """The same oracle over every host core: one single-threaded process per core, each
+    on its own sample of the workload (samples are independent), started with `spawn`
+    (the parent has a CUDA context). Aggregate rate = all bytes / the longest worker."""
+    import multiprocessing as mp
+    cores = max(1, min(os.cpu_count() or 1, max_workers))
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    try:
+        with mp.get_context("spawn").Pool(cores) as pool:
+            res = pool.map(_oracle_worker, [(wl.name, i, budget_s) for i in range(cores)])
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    total = sum(r[0] for r in res)
+    secs = max(r[1] for r in res)
+    return {"value": round(total / secs / 1e9, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{cores} processes, one per core (of {os.cpu_count()}), each repeating the oracle "
+                      f"on one sample of the workload ({sum(wl.numels):,} elements: noising + objective) "
+                      f"for about {budget_s:.0f} s; numpy float64, one thread per process"}
 
 
 def run_reference(args, wl: S.Workload, world: int):
@@ -1036,6 +1204,8 @@ def main():
                     help="untimed load before the warm-up steps so the GPU leaves its idle clocks")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-shapes", action="store_true",
+                    help="skip the objective-only rooflines at the 1024x1792 and sweep shapes")
     args = ap.parse_args()
     if args.warmup < 0 or args.steps < 1:
         ap.error("--steps >= 1 and --warmup >= 0")
@@ -1098,7 +1268,8 @@ def main():
     result = run_gpu(args, wl, rank, world, dist)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(wl, args.cpu_baseline_seconds)
+            result["cpu_baseline"] = cpu_baseline_all_cores(wl, args.cpu_baseline_seconds)
+            result["cpu_baseline_1core"] = cpu_baseline(wl, args.cpu_baseline_seconds)
         else:
             result["cpu_baseline"] = None
         print(json.dumps(result), flush=True)
