@@ -142,7 +142,7 @@ T_CLAMP = np.array([1e-3, math.pi / 2 - 1e-3], dtype=np.float32)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("mode", [S.SCM, S.STAGE3])
+@pytest.mark.parametrize("mode", [S.SCM, S.STAGE3, S.STAGE3_CFG])
 @pytest.mark.parametrize("gamma", [0.0, 0.5, 0.9, 1.0])
 @pytest.mark.parametrize("beta", [0.8, 1.0, 1.2])
 def test_clamp_boundary_timesteps(dtype, mode, gamma, beta):
@@ -151,7 +151,8 @@ def test_clamp_boundary_timesteps(dtype, mode, gamma, beta):
     (t -> 0, beta = 1), the gradient's 1/sin t is 1000, and with gamma = 1 the square
     root itself shrinks to cos t = 1e-3: the float32 per-sample coefficients must stay
     within the stated tolerances of the float64 oracle at both ends."""
-    inp = S.make_inputs(2, [20000, 333], dtype, S.STAGE3, seed=(310, int(gamma * 10), int(beta * 10)))
+    inp = S.make_inputs(2, [20000, 333], dtype, S.STAGE3_CFG if mode == S.STAGE3_CFG else S.STAGE3,
+                        seed=(310, int(gamma * 10), int(beta * 10)))
     p = Params(gamma=gamma, beta=beta)
     gpu = gpu_run(inp, p, mode, t_override=T_CLAMP)
     ref = oracle_run(inp, p, mode, t_override=T_CLAMP)
