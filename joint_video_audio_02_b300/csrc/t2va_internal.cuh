@@ -74,6 +74,7 @@ struct ObjectiveArgs {
   int vpc;                     // 16-byte vectors per chunk (a multiple of one CTA's batch)
   int nchunk[kMaxM];           // chunks per (sample, modality m) row
   int choff[kMaxM + 1];        // first chunk of modality m inside a sample; choff[M] = per sample
+  int out_m, out_c;            // the chunk of each sample that writes the per-sample outputs
 };
 
 struct NoiseArgs {

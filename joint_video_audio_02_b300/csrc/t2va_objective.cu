@@ -13,12 +13,14 @@
 //             directions g_sCM and g_DMD and accumulates sum g_sCM^2, sum |zhat0 - y_T|
 //             and sum g_DMD^2; the CTA adds them in a fixed order and writes the
 //             chunk's three partial sums to the workspace. The loads ask L2 to keep
-//             the inputs.
+//             the inputs. Before its dependency wait each CTA already requests the
+//             first vectors of its chunk into L2 (a bulk prefetch per input).
 //   k_grads : the same chunks. Each CTA starts the loads of its vectors again, except
 //             zhat0 (L2 hits; L2 may drop them now), adds the row's partial sums in chunk order
 //             (every CTA of a row gets bit-identical totals), derives the gradient
 //             factors, recomputes the directions and writes the float32 gradients
-//             once. The first chunk of each sample also writes the per-sample outputs.
+//             once. The sample's chunk with the fewest vectors also writes the
+//             per-sample outputs.
 //
 // HBM sees each input read once and each gradient written once when a call's inputs
 // fit in L2 (126 MB on B300; the stage-3 512x768 batch of 4 reads 45 MB); larger
@@ -35,6 +37,11 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kPerThread = 2;                    // vectors per thread per batch
 constexpr int kBatchVec = kThreads * kPerThread;  // vectors per CTA per batch
 constexpr int64_t kMaxWaveVec = 2048;             // longest chunk of a one-wave plan
+// Vectors at the start of a chunk that k_sums prefetches into L2 before its dependency
+// wait. Measured on B300 with caps of 192 to 384 vectors and with 1/8 to all of the
+// chunk: 256 to 320 is best at every stage-3 shape tried; prefetching more, or one batch
+// ahead inside the loop as well, loses.
+constexpr int64_t kEarlyVec = 320;
 
 template <typename T, int MODE>
 struct Traits {
@@ -86,6 +93,15 @@ __device__ __forceinline__ uint4 ld16(const void* p, uint64_t policy) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p), "l"(policy));
   return r;
+}
+
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned start) into L2 with an
+// eviction policy. It returns no data, so it may run before a dependency wait: L2 is
+// the point of coherence, and a later load still sees what the previous kernel wrote.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes),
+               "l"(policy)
+               : "memory");
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -373,14 +389,21 @@ __global__ void __launch_bounds__(kThreads, 3) k_sums(const __grid_constant__ Ob
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
   __shared__ float3 scratch[kWarps];
+  const Chunk k = chunk_of<VE>(a, blockIdx.x);
+  const uint64_t keep = policy_evict_last();
+  // The HBM stream starts while the previous kernel drains: thread q asks L2 for the
+  // chunk's first kEarlyVec vectors of input q. (Only a prefetch may run this early.)
+  if (threadIdx.x < Tr::NIN && k.v_hi > k.v_lo) {
+    const int64_t nv = min(k.v_hi - k.v_lo, kEarlyVec);
+    prefetch_l2(reinterpret_cast<const T*>(a.in[Tr::k0 + threadIdx.x][k.m]) + k.e_vec0 + k.v_lo * VE,
+                (uint32_t)(nv * 16), keep);
+  }
   // launched as a programmatic dependent of the previous kernel on the stream: no
-  // memory access before that kernel has finished; the next kernel (k_grads) may
-  // launch once every CTA of this one is past this point
+  // load before that kernel has finished; the next kernel (k_grads) may launch once
+  // every CTA of this one is past this point
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  const Chunk k = chunk_of<VE>(a, blockIdx.x);
   const Coefs cf = coefs_of<T, MODE>(a, k.b, k.m);
-  const uint64_t keep = policy_evict_last();
   float sg = 0.f, sa = 0.f, sd = 0.f;
   for (int64_t base = k.v_lo; base < k.v_hi; base += kBatchVec) {
     uint4 in[kPerThread][Tr::NIN];
@@ -416,16 +439,25 @@ __global__ void __launch_bounds__(kThreads, 3) k_sums(const __grid_constant__ Ob
 
 // Totals of row (b, m): the chunks' partial sums added in a fixed order (thread t
 // takes chunks t, t + 256, ...; then lanes; then warps), so every CTA of the row
-// gets the same bits.
+// gets the same bits. A thread's loads go two at a time, both in flight before it adds.
 __device__ __forceinline__ float3 row_totals(const ObjectiveArgs& a, int b, int m,
                                              float3 (&scratch)[kWarps]) {
   const float4* p = row_partials(a, b, m);
+  const int n = a.nchunk[m];
   float x = 0.f, y = 0.f, z = 0.f;
-  for (int c = threadIdx.x; c < a.nchunk[m]; c += kThreads) {
-    const float4 v = __ldcg(p + c);
-    x += v.x;
-    y += v.y;
-    z += v.z;
+#pragma unroll 1
+  for (int c0 = threadIdx.x; c0 < n; c0 += 2 * kThreads) {
+    const int c1 = c0 + kThreads;
+    const float4 v0 = __ldcg(p + c0);
+    const float4 v1 = c1 < n ? __ldcg(p + c1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    x += v0.x;
+    y += v0.y;
+    z += v0.z;
+    if (c1 < n) {
+      x += v1.x;
+      y += v1.y;
+      z += v1.z;
+    }
   }
   return block_sum3(x, y, z, scratch);
 }
@@ -492,12 +524,13 @@ __global__ void __launch_bounds__(kThreads, Traits<T, MODE>::kGradCtas)
     }
   }
 
-  // per-sample outputs: by the first chunk of the sample's first modality, from the
-  // totals of all its modalities (added in the same order as everywhere else)
-  if (k.m == 0 && k.c == 0) {
+  // per-sample outputs: by the sample's chunk with the fewest vectors (chunk out_c of
+  // modality out_m, chosen by the plan; it has time to spare), from the totals of all
+  // its modalities (added in the same order as everywhere else)
+  if (k.m == a.out_m && k.c == a.out_c) {
     float Ls = 0.f, Ld = 0.f;
     for (int m = 0; m < a.M; ++m) {
-      const float3 tm = m == 0 ? tot : row_totals(a, k.b, m, scratch);
+      const float3 tm = m == k.m ? tot : row_totals(a, k.b, m, scratch);
       if (threadIdx.x == 0) {
         if constexpr (Tr::kScm) {
           const float nm = sqrtf(tm.x);
@@ -599,12 +632,20 @@ bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int sm_count, ObjectiveLaun
     a.vpc = (int)(batches * kBatchVec);
   }
   int acc = 0;
+  int64_t fewest = INT64_MAX;
   for (int m = 0; m < a.M; ++m) {
     const int64_t nvec_ub = (a.n[m] + VE - 1) / VE;
     const int64_t c = std::max<int64_t>(1, (nvec_ub + a.vpc - 1) / a.vpc);  // >= 1: edges
     a.nchunk[m] = (int)c;
     a.choff[m] = acc;
     acc += (int)c;
+    // the per-sample outputs go to the row's last (shortest) chunk with the fewest vectors
+    const int64_t last = nvec_ub - (c - 1) * a.vpc;
+    if (last < fewest) {
+      fewest = last;
+      a.out_m = m;
+      a.out_c = (int)c - 1;
+    }
   }
   for (int m = a.M; m <= kMaxM; ++m) a.choff[m] = acc;
   const int64_t grid = (int64_t)a.B * acc;
