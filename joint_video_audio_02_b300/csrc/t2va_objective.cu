@@ -9,7 +9,7 @@
 //   k_sums  : every (sample, modality) row is cut into chunks of `vpc` 16-byte
 //             vectors, one CTA per chunk (rows of every sample and modality in one
 //             grid, so the small audio rows share the GPU with the video rows). Each
-//             thread issues all the loads of its vectors at once, computes the float32
+//             thread keeps the loads of two of its vectors in flight, computes the float32
 //             directions g_sCM and g_DMD and accumulates sum g_sCM^2, sum |zhat0 - y_T|
 //             and sum g_DMD^2; the CTA adds them in a fixed order and writes the
 //             chunk's three partial sums to the workspace. The loads ask L2 to keep
@@ -404,22 +404,26 @@ __global__ void __launch_bounds__(kThreads, 3) k_sums(const __grid_constant__ Ob
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const Coefs cf = coefs_of<T, MODE>(a, k.b, k.m);
+  // Thread t takes vectors t, t + 256, t + 512, ... of the chunk, two at a time in
+  // flight: while it forms the directions of one vector, the loads of the next are out,
+  // and each vector's loads are reissued for the vector two steps ahead once it is used.
   float sg = 0.f, sa = 0.f, sd = 0.f;
-  for (int64_t base = k.v_lo; base < k.v_hi; base += kBatchVec) {
-    uint4 in[kPerThread][Tr::NIN];
-#pragma unroll
-    for (int u = 0; u < kPerThread; ++u) {  // every load of the batch first
-      const int64_t v = base + u * kThreads + threadIdx.x;
-      if (v < k.v_hi) load_vec<T, MODE>(in[u], a, k.m, k.e_vec0 + v * VE, keep);
+  uint4 A[Tr::NIN], B[Tr::NIN];
+  int64_t v = k.v_lo + threadIdx.x;
+  if (v < k.v_hi) load_vec<T, MODE>(A, a, k.m, k.e_vec0 + v * VE, keep);
+  if (v + kThreads < k.v_hi) load_vec<T, MODE>(B, a, k.m, k.e_vec0 + (v + kThreads) * VE, keep);
+  for (; v < k.v_hi; v += 2 * kThreads) {
+    const int64_t v1 = v + kThreads, v2 = v + 2 * kThreads, v3 = v + 3 * kThreads;
+    {
+      float gs[VE], gd[VE];
+      directions<T, MODE>(A, cf, gs, gd, sg, sa, sd);
     }
-#pragma unroll
-    for (int u = 0; u < kPerThread; ++u) {
-      const int64_t v = base + u * kThreads + threadIdx.x;
-      if (v < k.v_hi) {
-        float gs[VE], gd[VE];
-        directions<T, MODE>(in[u], cf, gs, gd, sg, sa, sd);
-      }
+    if (v2 < k.v_hi) load_vec<T, MODE>(A, a, k.m, k.e_vec0 + v2 * VE, keep);
+    if (v1 < k.v_hi) {
+      float gs[VE], gd[VE];
+      directions<T, MODE>(B, cf, gs, gd, sg, sa, sd);
     }
+    if (v3 < k.v_hi) load_vec<T, MODE>(B, a, k.m, k.e_vec0 + v3 * VE, keep);
   }
   const int64_t e = edge_element<VE>(a, k);
   if (e >= 0) {

@@ -314,6 +314,64 @@ def test_cuda_graph_capture_matches_eager():
         assert torch.equal(a, b)
 
 
+def test_objective_right_after_the_noising_that_writes_its_input():
+    """The noising kernel lets its dependents launch early, and the objective's first
+    kernel starts pulling its inputs into L2 before its dependency wait. Here the
+    noising overwrites z_t (holding the previous iteration's values) immediately before
+    the objective reads it, on one stream with no synchronisation: the results must be
+    bit-identical to the objective run on a settled copy of that z_t, and match the
+    float64 oracle on it."""
+    wl = S.workload("stage3_512x768_bf16")
+    inp = _inputs(wl.name)
+    p = Params.of(wl)
+    dt = wl.dtype
+    z0, eps, xT, xS, tan, zh, yT, yF = (to_device(getattr(inp, f), dt) for f in (
+        "z0", "eps", "x0_teacher", "x0_student", "x0_tangent", "zhat0", "x0_teacher_hat", "x0_fake"))
+    zt = alloc_like(z0)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = t2va.new_workspace(wl.batch, 2)
+
+    def objective(z, t):
+        gS, gD = grads_like(z0, float("nan")), grads_like(z0, float("nan"))
+        loss, loss_s, loss_d = (torch.full((wl.batch,), float("nan"), device="cuda") for _ in range(3))
+        norm = torch.full((wl.batch * 2,), float("nan"), device="cuda")
+        cdmd = torch.full((wl.batch * 2,), float("nan"), device="cuda")
+        t2va.stage3_objective(z, xT, xS, tan, t, zh, yT, yF, beta=p.beta, gamma=p.gamma,
+                              eps_scm=p.eps_scm, eps_dmd=p.eps_dmd, weight=p.weight,
+                              lambda_scm=p.lambda_scm, lambda_dmd=p.lambda_dmd, grad_x0_student=gS,
+                              grad_zhat0=gD, loss=loss, loss_scm=loss_s, loss_dmd=loss_d, norm=norm,
+                              cdmd=cdmd, workspace=ws, status=st)
+        return (loss, loss_s, loss_d, norm, cdmd), gS, gD
+
+    rng = np.random.default_rng(41)
+    for it in range(4):
+        t_host = rng.uniform(0.05, 1.5, wl.batch).astype(np.float32)
+        t = torch.from_numpy(t_host).cuda()
+        torch.cuda.synchronize()
+        t2va.noise(z0, eps, zt, t, status=st)         # overwrites last iteration's z_t
+        chained = objective(zt, t)                    # same stream, no synchronisation
+        torch.cuda.synchronize()
+        settled_zt = [z.clone() for z in zt]
+        torch.cuda.synchronize()
+        settled = objective(settled_zt, t)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        for a, b in zip(chained[0], settled[0]):
+            assert torch.equal(a, b), it
+        for a, b in zip(chained[1] + chained[2], settled[1] + settled[2]):
+            assert torch.equal(a, b), it
+    # the last chained call against the oracle on the z_t the noising wrote
+    zt_bits = [z.view(torch.int16).cpu().numpy().view(np.uint16) for z in zt]
+    ref = oracle.stage3_objective(zt_bits, inp.x0_teacher, inp.x0_student, inp.x0_tangent, t_host,
+                                  inp.zhat0, inp.x0_teacher_hat, inp.x0_fake, p.beta, p.gamma,
+                                  p.eps_scm, p.eps_dmd, p.weight, p.lambda_scm, p.lambda_dmd, dt)
+    (loss, loss_s, loss_d, norm, cdmd), gS, gD = chained
+    compare({"loss": loss.cpu().numpy(), "loss_scm": loss_s.cpu().numpy(), "loss_dmd": loss_d.cpu().numpy(),
+             "norm": norm.cpu().numpy().reshape(wl.batch, 2), "cdmd": cdmd.cpu().numpy().reshape(wl.batch, 2),
+             "grad_x0_student": [g.cpu().numpy() for g in gS],
+             "grad_zhat0": [g.cpu().numpy() for g in gD]}, ref, dt, S.STAGE3)
+
+
 # --------------------------------------------------------------------------
 # the workspace: per-chunk partial sums written and read within one call
 # --------------------------------------------------------------------------
