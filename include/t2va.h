@@ -62,7 +62,8 @@
 extern "C" {
 #endif
 
-#define T2VA_ABI_VERSION 2  /* 2: t2va_noise_rf, t2va_stage3_objective_cfg, W8A8, t2va_residual_modnorm */
+#define T2VA_ABI_VERSION 3  /* 2: t2va_noise_rf, t2va_stage3_objective_cfg, W8A8, t2va_residual_modnorm;
+                               3: t2va_objective_plan_query */
 #define T2VA_MAX_MODALITIES 4
 
 typedef enum t2va_dtype {
@@ -112,6 +113,40 @@ int t2va_abi_version(void);
  * may run concurrently need distinct workspaces. Returns 0 on invalid arguments
  * or if no device can be queried. */
 size_t t2va_workspace_bytes(int batch, int num_modalities);
+
+/* The launch plan of an objective call (t2va_scm_objective, t2va_dmd_objective and the
+ * t2va_stage3_objective family) for these sizes on a GPU with `sm_count` SMs. Host
+ * arithmetic only: no device is touched and nothing is enqueued, so it runs without a
+ * GPU. The plan depends only on the arguments given here.
+ *
+ * Each (sample, modality) row is cut into chunks of `vectors_per_chunk` 16-byte
+ * vectors (8 bfloat16 or 4 float32 elements; the unaligned head and tail elements of a
+ * sample go to its first and last chunk); both kernels of a call launch one CTA per
+ * chunk of every row of every sample.
+ *   grid               CTAs per kernel: batch * sum_m chunks[m]
+ *   threads            threads per CTA
+ *   vectors_per_chunk  16-byte vectors per chunk
+ *   chunks[m]          chunks per row of modality m, 1 ... 1024 (entries past
+ *                      num_modalities are 0)
+ *   outputs_modality, outputs_chunk
+ *                      the chunk of every sample whose CTA also writes the per-sample
+ *                      outputs (loss, norm, cdmd): the shortest last chunk of a row
+ *   one_wave           1 when the grid fits in one wave of three CTAs per SM
+ * Returns T2VA_SUCCESS, T2VA_ERROR_INVALID_ARGUMENT (a geometry the objective entry
+ * points reject, sm_count < 1, a null `out`, or sizes no plan covers) or
+ * T2VA_ERROR_UNSUPPORTED_DTYPE. */
+typedef struct t2va_objective_plan {
+  int grid;
+  int threads;
+  int vectors_per_chunk;
+  int chunks[T2VA_MAX_MODALITIES];
+  int outputs_modality;
+  int outputs_chunk;
+  int one_wave;
+} t2va_objective_plan;
+
+int t2va_objective_plan_query(int batch, int num_modalities, const t2va_segment* seg,
+                              t2va_dtype dtype, int sm_count, t2va_objective_plan* out);
 
 /* Zero a workspace (16-byte aligned device memory of `workspace_bytes`) on
  * `stream` and write its header. Optional: the objective entry points do not

@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     new_workspace,
     noise,
     noise_rf,
+    objective_plan,
     quantize_rows,
     residual_modnorm,
     scm_objective,

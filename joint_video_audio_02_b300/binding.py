@@ -38,11 +38,17 @@ EXPORTED = ("t2va_error_string", "t2va_abi_version", "t2va_workspace_bytes", "t2
             "t2va_noise", "t2va_scm_objective", "t2va_dmd_objective", "t2va_stage3_objective",
             "t2va_stage3_objective_noalloc", "t2va_noise_rf", "t2va_stage3_objective_cfg",
             "t2va_quantize_rows", "t2va_w8a8_linear", "t2va_selftest_wait_timeout",
-            "t2va_residual_modnorm")
+            "t2va_residual_modnorm", "t2va_objective_plan_query")
 
 
 class Segment(ctypes.Structure):
     _fields_ = [("numel", c_int64), ("sample_stride", c_int64)]
+
+
+class ObjectivePlan(ctypes.Structure):
+    _fields_ = [("grid", c_int), ("threads", c_int), ("vectors_per_chunk", c_int),
+                ("chunks", c_int * MAX_MODALITIES), ("outputs_modality", c_int),
+                ("outputs_chunk", c_int), ("one_wave", c_int)]
 
 
 class T2VAError(RuntimeError):
@@ -96,6 +102,8 @@ def _declare(lib):
     lib.t2va_selftest_wait_timeout.restype = c_int
     lib.t2va_residual_modnorm.argtypes = [c_int64, c_int64, c_int64, c_int, P, P, P, P, P, c_float, P, P, P]
     lib.t2va_residual_modnorm.restype = c_int
+    lib.t2va_objective_plan_query.argtypes = [c_int, c_int, seg, c_int, c_int, ctypes.POINTER(ObjectivePlan)]
+    lib.t2va_objective_plan_query.restype = c_int
 
 
 def load(path: Optional[str] = None):
@@ -173,6 +181,25 @@ def _opt(t: Optional[torch.Tensor]):
 def _f32(t: torch.Tensor, name: str):
     if t.dtype != torch.float32 or not t.is_cuda:
         raise TypeError(f"{name} must be a float32 CUDA tensor")
+
+
+def objective_plan(batch: int, numels: Sequence[int], dtype: str, sm_count: int,
+                   sample_strides: Optional[Sequence[int]] = None) -> dict:
+    """The launch plan of an objective call with these sizes (t2va_objective_plan_query):
+    host arithmetic only, no device needed. `dtype` is "bf16" or "f32"; strides default
+    to the numels (contiguous samples)."""
+    M = len(numels)
+    strides = list(numels) if sample_strides is None else list(sample_strides)
+    segs = (Segment * M)()
+    for m in range(M):
+        segs[m].numel, segs[m].sample_stride = int(numels[m]), int(strides[m])
+    code = {"bf16": T2VA_BFLOAT16, "f32": T2VA_FLOAT32}.get(dtype, -1)
+    out = ObjectivePlan()
+    _check(load().t2va_objective_plan_query(int(batch), M, segs, code, int(sm_count), ctypes.byref(out)),
+           "t2va_objective_plan_query")
+    return {"grid": out.grid, "threads": out.threads, "vectors_per_chunk": out.vectors_per_chunk,
+            "chunks": [out.chunks[m] for m in range(M)], "outputs_modality": out.outputs_modality,
+            "outputs_chunk": out.outputs_chunk, "one_wave": bool(out.one_wave)}
 
 
 def workspace_bytes(batch: int, num_modalities: int) -> int:

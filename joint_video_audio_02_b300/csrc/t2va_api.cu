@@ -125,7 +125,7 @@ int run_objective(ObjectiveArgs& a, t2va_dtype dt, int mode, const WsRef& ws,
     if (s_ok && d_ok) a.wide_mask |= 1u << m;
   }
   ObjectiveLaunch l;
-  if (!plan_objective(a, dt, dev.sm_count, &l)) return T2VA_ERROR_CUDA;
+  if (!plan_objective(a, dt, dev.sm_count, &l)) return T2VA_ERROR_INVALID_ARGUMENT;
   const cudaError_t e = launch_objective(a, dt, mode, l, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -280,6 +280,26 @@ const char* t2va_error_string(int code) {
 }
 
 int t2va_abi_version(void) { return T2VA_ABI_VERSION; }
+
+int t2va_objective_plan_query(int batch, int num_modalities, const t2va_segment* seg,
+                              t2va_dtype dtype, int sm_count, t2va_objective_plan* out) {
+  T2VA_TRY(check_geometry(batch, num_modalities, seg));
+  T2VA_TRY(check_dtype(dtype));
+  if (sm_count < 1 || out == nullptr) return T2VA_ERROR_INVALID_ARGUMENT;
+  ObjectiveArgs a;
+  fill_geometry(a, batch, num_modalities, seg);
+  ObjectiveLaunch l;
+  if (!plan_objective(a, dtype, sm_count, &l)) return T2VA_ERROR_INVALID_ARGUMENT;
+  std::memset(out, 0, sizeof(*out));
+  out->grid = l.grid;
+  out->threads = l.threads;
+  out->vectors_per_chunk = a.vpc;
+  for (int m = 0; m < num_modalities; ++m) out->chunks[m] = a.nchunk[m];
+  out->outputs_modality = a.out_m;
+  out->outputs_chunk = a.out_c;
+  out->one_wave = (int64_t)l.grid <= 3 * (int64_t)sm_count ? 1 : 0;
+  return T2VA_SUCCESS;
+}
 
 size_t t2va_workspace_bytes(int batch, int num_modalities) {
   if (batch < 0 || num_modalities < 1 || num_modalities > kMaxM) return 0;

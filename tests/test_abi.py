@@ -40,7 +40,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_error_strings(lib):
-    assert lib.t2va_abi_version() == 2
+    assert lib.t2va_abi_version() == 3
     for code in range(0, 7):
         assert len(t2va.error_string(code)) > 5
 
