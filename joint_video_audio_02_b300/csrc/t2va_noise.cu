@@ -20,6 +20,12 @@ namespace {
 constexpr int kNoiseThreads = 256;
 constexpr int kNoiseUnroll = 4;
 constexpr int kNoiseVecPerCta = kNoiseThreads * kNoiseUnroll;
+// Vectors of each input a CTA prefetches into L2 before its dependency wait. Measured on
+// B300 in the stage-3 512x768 step (noising of four latents beside the objective): 256,
+// 384, 512, 640 and 1024 vectors gave 21.24, 21.21, 21.17, 21.15 and 21.30 us per step
+// against 21.35 without; back to back the noising alone took 6.64, 6.87, 7.02, 7.25 and
+// 7.29 us against 7.34.
+constexpr int64_t kNoiseEarlyVec = 512;
 
 // The noised samples are read next by the objective: their lines are stored with an
 // evict_last L2 policy so that they are still there when it reads them (measured
@@ -77,8 +83,32 @@ __global__ void __launch_bounds__(kNoiseThreads) k_noise(const __grid_constant__
   constexpr int VE = Vec<T>::VE;
   const int bid = blockIdx.x;
 
+  // The HBM stream starts while the previous kernel drains: threads 0 and 1 ask L2 for
+  // the first kNoiseEarlyVec vectors of this CTA's z0 and eps (a bulk prefetch returns
+  // nothing to the SM and L2 is the point of coherence, so it may run before the wait).
+  if (threadIdx.x < 2 && bid < a.block_off[a.M]) {
+    int m = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxM; ++i)
+      if (i < a.M && bid >= a.block_off[i]) m = i;
+    const int local = bid - a.block_off[m];
+    const int b = local / a.chunks[m];
+    const SegGeom g = seg_geom<VE>(a.n[m], a.stride[m], b);
+    const int64_t vbeg = (int64_t)(local - b * a.chunks[m]) * kNoiseVecPerCta;
+    int64_t nv = g.nvec - vbeg;
+    if (nv > kNoiseEarlyVec) nv = kNoiseEarlyVec;
+    if (nv > 0) {
+      const T* p = reinterpret_cast<const T*>(threadIdx.x == 0 ? a.z0[m] : a.eps[m]) + g.e0 + g.head +
+                   vbeg * VE;
+      uint64_t first;
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(first));
+      asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p),
+                   "r"((uint32_t)(nv * 16)), "l"(first)
+                   : "memory");
+    }
+  }
   // launched as a programmatic dependent of the previous kernel on the stream: no
-  // memory access before that kernel has finished
+  // load before that kernel has finished
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
 
