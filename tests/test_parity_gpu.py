@@ -372,6 +372,45 @@ def test_objective_right_after_the_noising_that_writes_its_input():
              "grad_zhat0": [g.cpu().numpy() for g in gD]}, ref, dt, S.STAGE3)
 
 
+def test_noising_right_after_the_objective_that_writes_its_input():
+    """The noising kernel also pulls its inputs into L2 before its dependency wait. Here
+    its z0 and eps are the float32 gradients that the objective's second kernel (which
+    lets its dependents launch early) writes immediately before, on one stream with no
+    synchronisation: z_t must be bit-identical to the noising of a settled copy."""
+    wl = S.workload("stage3_512x768_bf16")
+    inp = _inputs(wl.name)
+    p = Params.of(wl)
+    dt = wl.dtype
+    zt_in, xT, xS, tan, zh, yT, yF = (to_device(getattr(inp, f), dt) for f in (
+        "z0", "x0_teacher", "x0_student", "x0_tangent", "zhat0", "x0_teacher_hat", "x0_fake"))
+    t = torch.from_numpy(inp.t).cuda()
+    gS, gD = grads_like(zt_in, float("nan")), grads_like(zt_in, float("nan"))
+    out = grads_like(zt_in, float("nan"))
+    loss = torch.zeros(wl.batch, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = t2va.new_workspace(wl.batch, 2)
+    rng = np.random.default_rng(43)
+    for it in range(4):
+        w = [float(x) for x in rng.uniform(0.5, 2.0, 2)]
+        t_noise = torch.from_numpy(rng.uniform(0.05, 1.5, wl.batch).astype(np.float32)).cuda()
+        torch.cuda.synchronize()
+        t2va.stage3_objective(zt_in, xT, xS, tan, t, zh, yT, yF, beta=p.beta, gamma=p.gamma,
+                              eps_scm=p.eps_scm, eps_dmd=p.eps_dmd, weight=w,
+                              lambda_scm=p.lambda_scm, lambda_dmd=p.lambda_dmd, grad_x0_student=gS,
+                              grad_zhat0=gD, loss=loss, workspace=ws, status=st)
+        t2va.noise(gS, gD, out, t_noise, status=st)   # same stream, no synchronisation
+        torch.cuda.synchronize()
+        chained = [o.clone() for o in out]
+        settled_in = ([g.clone() for g in gS], [g.clone() for g in gD])
+        torch.cuda.synchronize()
+        t2va.noise(settled_in[0], settled_in[1], out, t_noise, status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        for a, b in zip(chained, out):
+            assert torch.equal(a, b), it
+            assert torch.isfinite(a).all(), it
+
+
 # --------------------------------------------------------------------------
 # the workspace: per-chunk partial sums written and read within one call
 # --------------------------------------------------------------------------
