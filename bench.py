@@ -644,7 +644,8 @@ def run_e2e(args, wl, host0, status, noise, objective, dev, nb, world, dist):
     device block that is read back whole. Steps are pipelined the way a data loader
     feeds a training loop: two device buffer sets alternate, and the copies in, the
     compute and the copies out run on three streams ordered by events, so step i+1's
-    inputs arrive while step i computes and step i-1's results drain."""
+    inputs arrive while step i computes and step i-1's results drain. The host's time to
+    submit a step is reported beside the device time."""
     import torch
 
     steps = max(4, min(args.steps, args.e2e_steps))
@@ -729,15 +730,18 @@ def run_e2e(args, wl, host0, status, noise, objective, dev, nb, world, dist):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(s_in)
+    t_host = time.perf_counter()
     for i in range(steps):
         step(i)
     e1.record(s_out)
+    host_ms = (time.perf_counter() - t_host) * 1e3 / steps
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     assert int(status.item()) == 0
     return {"value": round(whole_job_gbs(world, nb["step"], steps, ms), 3), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": ms / steps,
+            "host_submit_ms_per_step": round(host_ms, 4),
             "link_gbs_per_step": round((h2d + d2h) / (ms / steps * 1e-3) / 1e9, 2),
             "pipeline": "2 device buffer sets; copy-in, compute and copy-out streams; one "
                         "pinned-block copy per direction per step",
