@@ -86,6 +86,8 @@ __global__ void __launch_bounds__(kNoiseThreads) k_noise(const __grid_constant__
   // The HBM stream starts while the previous kernel drains: threads 0 and 1 ask L2 for
   // the first kNoiseEarlyVec vectors of this CTA's z0 and eps (a bulk prefetch returns
   // nothing to the SM and L2 is the point of coherence, so it may run before the wait).
+  // Only these two threads work out the chunk here; the whole CTA does it again after
+  // the wait (doing it once, for every thread, before the wait measured 0.66 us slower).
   if (threadIdx.x < 2 && bid < a.block_off[a.M]) {
     int m = 0;
 #pragma unroll
