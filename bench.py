@@ -266,7 +266,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 EXTRA_SHAPES = ["stage3_1024x1792_bf16", "stage3_sweep_b1_bf16", "stage3_sweep_b4_bf16",
-                "stage3_sweep_b16_bf16", "stage3_sweep_b32_bf16"]
+                "stage3_sweep_b16_bf16", "stage3_sweep_b32_bf16", "scm_512x768_bf16"]
 
 
 def objective_rooflines(names, dev, cap_stream, n_launch, l2, peak):
@@ -284,7 +284,8 @@ def objective_rooflines(names, dev, cap_stream, n_launch, l2, peak):
         w = S.workload(name)
         tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
         n_el = w.batch * sum(w.numels)
-        nbytes = n_el * bytes_per_element("stage3", w.dtype)
+        scm_only = w.mode == S.SCM
+        nbytes = n_el * bytes_per_element("scm" if scm_only else "stage3", w.dtype)
         R = max(2, math.ceil(3 * l2 / (nbytes + 2 * n_el * elem_size(w.dtype))))
         g = torch.Generator(device=dev)
         g.manual_seed(1234)
@@ -301,6 +302,12 @@ def objective_rooflines(names, dev, cap_stream, n_launch, l2, peak):
         st = torch.zeros(1, dtype=torch.int32, device=dev)
 
         def call(d):
+            if scm_only:
+                t2va.scm_objective(d["zt"], d["xT"], d["xS"], d["tan"], d["t"], beta=w.beta,
+                                   gamma=w.gamma, eps_scm=w.eps_scm, weight=w.weight,
+                                   lambda_scm=w.lambda_scm, grad_x0_student=d["gS"], loss=d["loss"],
+                                   workspace=ws, status=st, stream=cap_stream)
+                return
             t2va.stage3_objective(d["zt"], d["xT"], d["xS"], d["tan"], d["t"], d["zh"], d["yT"], d["yF"],
                                   beta=w.beta, gamma=w.gamma, eps_scm=w.eps_scm, eps_dmd=w.eps_dmd,
                                   weight=w.weight, lambda_scm=w.lambda_scm, lambda_dmd=w.lambda_dmd,
@@ -1211,7 +1218,7 @@ def main():
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra-shapes", action="store_true",
-                    help="skip the objective-only rooflines at the 1024x1792 and sweep shapes")
+                    help="skip the objective-only rooflines at the 1024x1792, sweep and sCM-only shapes")
     args = ap.parse_args()
     if args.warmup < 0 or args.steps < 1:
         ap.error("--steps >= 1 and --warmup >= 0")
