@@ -611,17 +611,25 @@ bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int sm_count, ObjectiveLaun
   }
   grid1 *= a.B;
   total *= a.B;
-  const int64_t resident = 3 * (int64_t)std::max(1, sm_count);
-  if (total <= resident * kMaxWaveVec) {
+  const int64_t sms = std::max(1, sm_count);
+  const int64_t resident = 3 * sms;
+  // A one-wave plan leaves about one slot in 28 free (16 of 444 on B300): the CTAs of
+  // the next kernel on the stream, or of a kernel on another stream, start there while
+  // this one drains. Measured on B300 against a full wave: the stage-3 512x768 step with
+  // the next steps' noising beside it 21.07 -> 20.78 us, the objective alone 15.88 ->
+  // 15.93 us (512x768) and 19.02 -> 18.96 us (1024x1792); 24 to 72 free slots helped the
+  // step more but cost the objective 0.2 to 1.4 us.
+  const int64_t wave = resident - sms / 9;
+  if (total <= wave * kMaxWaveVec) {
     // One balanced wave: the shortest chunk (a multiple of 32 vectors) that gives at most
-    // one CTA per resident slot (three per SM), so every SM gets three nearly equal
-    // chunks (measured on B300: 1024x1792 batch 1 23.2 -> 21.3 us; 512x768 batch 4 18.3).
-    int64_t vpc = std::max<int64_t>(32, ((total + resident - 1) / resident + 31) / 32 * 32);
+    // `wave` CTAs, so the SMs get nearly equal chunks, three on most of them (measured on
+    // B300: 1024x1792 batch 1 23.2 -> 21.3 us; 512x768 batch 4 18.3).
+    int64_t vpc = std::max<int64_t>(32, ((total + wave - 1) / wave + 31) / 32 * 32);
     for (;;) {
       int64_t g = 0;
       for (int m = 0; m < a.M; ++m)
         g += std::max<int64_t>(1, ((a.n[m] + VE - 1) / VE + vpc - 1) / vpc);
-      if (a.B * g <= resident || vpc >= kMaxWaveVec) break;
+      if (a.B * g <= wave || vpc >= kMaxWaveVec) break;
       vpc += 32;
     }
     a.vpc = (int)vpc;
