@@ -17,14 +17,19 @@
 namespace t2va {
 namespace {
 
-constexpr int kNoiseThreads = 256;
-constexpr int kNoiseUnroll = 4;
+// Small CTAs: 128 threads of at most 32 registers (4096 registers a CTA) fit on an SM
+// beside three CTAs of the objective kernels (3 x 256 threads x 80 registers), so the
+// noising of the next steps runs on every SM while an objective call streams. Measured on
+// B300 in the stage-3 512x768 step: 256 threads x 4 vectors (40-56 registers) 20.84 us,
+// 256 x 2 20.74 us, 128 x 4 20.95 us, 128 x 2 20.55 us; the noising alone 7.01, 7.32, 7.83
+// and 7.10 us.
+constexpr int kNoiseThreads = 128;
+constexpr int kNoiseUnroll = 2;
 constexpr int kNoiseVecPerCta = kNoiseThreads * kNoiseUnroll;
-// Vectors of each input a CTA prefetches into L2 before its dependency wait. Measured on
-// B300 in the stage-3 512x768 step (noising of four latents beside the objective): 256,
-// 384, 512, 640 and 1024 vectors gave 21.24, 21.21, 21.17, 21.15 and 21.30 us per step
-// against 21.35 without; back to back the noising alone took 6.64, 6.87, 7.02, 7.25 and
-// 7.29 us against 7.34.
+// Vectors of each input a CTA prefetches into L2 before its dependency wait: with 256
+// vectors a CTA, all of them. (Measured on B300 with 1024-vector CTAs in the stage-3
+// 512x768 step: 256, 384, 512, 640 and 1024 vectors gave 21.24, 21.21, 21.17, 21.15 and
+// 21.30 us per step against 21.35 without.)
 constexpr int64_t kNoiseEarlyVec = 512;
 
 // The noised samples are read next by the objective: their lines are stored with an
@@ -78,8 +83,11 @@ __device__ __forceinline__ float mix(float cz, float z, float ce, float e) {
   return fmaf(cz, z, ce * e);
 }
 
+// 16 CTAs an SM caps a thread at 32 registers; the kernel writing both z_t and z_rf gets
+// 42 (12 CTAs), since at 32 it spills and ran 10.5 instead of 8.3 us.
 template <typename T, int OUT>
-__global__ void __launch_bounds__(kNoiseThreads) k_noise(const __grid_constant__ NoiseArgs a) {
+__global__ void __launch_bounds__(kNoiseThreads, OUT == (kNoiseZt | kNoiseRf) ? 12 : 16)
+    k_noise(const __grid_constant__ NoiseArgs a) {
   constexpr int VE = Vec<T>::VE;
   const int bid = blockIdx.x;
 
