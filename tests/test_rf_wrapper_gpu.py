@@ -116,6 +116,47 @@ def test_noise_rf_ragged(dtype, case):
             assert torch.all(gap == 7.0)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("case", RAGGED, ids=[f"B{b}-{'-'.join(map(str, n))}-p{p}" for b, n, p in RAGGED])
+def test_noise_zt_ragged_both_kernels(dtype, case):
+    """z_t on the same ragged geometries, from the z_t-only kernel and from the kernel that
+    writes z_t and z_rf together (their own instantiations, with their own register caps):
+    z_t within the float32 evaluation bound of cos t z0 + sin t eps (one output ulp plus
+    8 * 2^-24 of the magnitudes, as in the noise parity test), the two kernels' z_t equal
+    bit for bit, z_rf within its bound, and the padding between strided samples untouched."""
+    B, numels, pad = case
+    inp = S.make_inputs(B, numels, dtype, S.SCM, seed=(503, B, len(numels), pad))
+    z0 = to_device(inp.z0, dtype, pad)
+    eps = to_device(inp.eps, dtype, pad)
+    t = torch.from_numpy(inp.t).cuda()
+    zt = alloc_like(z0, fill=7.0)
+    zt2 = alloc_like(z0, fill=7.0)
+    zrf = alloc_like(z0, fill=7.0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t2va.noise(z0, eps, zt, t, status=status)
+    t2va.noise_rf(z0, eps, zt2, zrf, t, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    got = to_host(zt, dtype)
+    t64 = inp.t.astype(np.float64)[:, None]
+    for m in range(len(got)):
+        z = oracle.decode(inp.z0[m], dtype)
+        e = oracle.decode(inp.eps[m], dtype)
+        exact = np.cos(t64) * z + np.sin(t64) * e
+        mag = np.abs(np.cos(t64) * z) + np.abs(np.sin(t64) * e)
+        g = oracle.decode(got[m], dtype)
+        bound = _ulp(exact, dtype) + 8 * 2.0 ** -24 * mag
+        assert np.all(np.abs(g - exact) <= bound), \
+            f"z_t modality {m}: worst {np.max(np.abs(g - exact) / bound):.2f} of bound"
+    for a, b in zip(zt, zt2):
+        assert torch.equal(a, b)
+    _check_rf(inp, to_host(zrf, dtype), None, inp.t)
+    if pad and B > 1:
+        for x in zt + zt2 + zrf:
+            gap = x.as_strided((B, x.stride(0) - x.shape[1]), (x.stride(0), 1), x.shape[1])
+            assert torch.all(gap == 7.0)
+
+
 def test_noise_rf_in_place_and_empty_modality():
     """z_rf written over z0 (in place), and t_rf written even when no modality has an
     element (the launch then has one CTA per sample)."""
