@@ -485,9 +485,12 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
     reps, rem = divmod(K, S_steps)
     g_rem = capture(rem, offset=S_steps) if rem else None
     g_warm = capture(max(W, 3))
-    # the dominant kernel alone: back-to-back objective launches over the same rotating sets
-    g_obj = capture(S_steps, objective_only=True)
-    g_noise = capture(S_steps, noise_only=True)
+    # the dominant kernel alone: back-to-back objective launches over the same rotating sets,
+    # in graphs of at least 500 launches whatever K is, so that a graph's fixed launch cost
+    # is not spread over a handful of launches (at --steps 20 it added 0.3 us to each)
+    S_leg = max(S_steps, 500)
+    g_obj = capture(S_leg, objective_only=True)
+    g_noise = capture(S_leg, noise_only=True)
     torch.cuda.synchronize()
 
     # The clock sampler runs from before the clock ramp to after the per-kernel legs, so
@@ -529,8 +532,9 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
         raise RuntimeError(f"device status {st} during the benchmark")
 
     # the objective's mean launch duration: CUDA events on the launching stream around
-    # `obj_reps` replays of S_steps back-to-back launches (inputs rotate over R sets)
-    obj_reps = max(1, min(reps, 10))
+    # `obj_reps` replays of S_leg back-to-back launches (inputs rotate over R sets), about
+    # 5000 launches in all
+    obj_reps = max(1, 5000 // S_leg)
     o_start = torch.cuda.Event(enable_timing=True)
     o_end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(cap_stream):
@@ -540,7 +544,7 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
             g_obj.replay()
         o_end.record(cap_stream)
     cap_stream.synchronize()
-    obj_mean_ms = o_start.elapsed_time(o_end) / (obj_reps * S_steps)
+    obj_mean_ms = o_start.elapsed_time(o_end) / (obj_reps * S_leg)
     # the same for the noising kernel
     with torch.cuda.stream(cap_stream):
         g_noise.replay()
@@ -549,13 +553,13 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
             g_noise.replay()
         o_end.record(cap_stream)
     cap_stream.synchronize()
-    noise_mean_ms = o_start.elapsed_time(o_end) / (obj_reps * S_steps)
+    noise_mean_ms = o_start.elapsed_time(o_end) / (obj_reps * S_leg)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during the benchmark")
     peak, peak_kind = measured_peak()
     extra = None
     if wl.name == DEFAULT_WORKLOAD and not args.no_extra_shapes:
-        extra = objective_rooflines(EXTRA_SHAPES, dev, cap_stream, min(S_steps, 100), l2, peak)
+        extra = objective_rooflines(EXTRA_SHAPES, dev, cap_stream, 100, l2, peak)
     h2 = time.time()
     time.sleep(0.02)
     sampler.stop()
@@ -604,7 +608,7 @@ def run_gpu(args, wl: S.Workload, rank: int, world: int, dist):
                      "traffic": committed_traffic(wl.name),
                      "algorithmic_bytes_per_launch": nb["objective"],
                      "mean_launch_us": round(obj_mean_ms * 1e3, 3),
-                     "launches_timed": obj_reps * S_steps,
+                     "launches_timed": obj_reps * S_leg,
                      "launch_timing": "back-to-back objective launches in a CUDA graph, CUDA events "
                                       "around the region on the launching stream; includes the "
                                       "launch-to-launch gap",
