@@ -404,9 +404,10 @@ __global__ void __launch_bounds__(kThreads, 3) k_sums(const __grid_constant__ Ob
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const Coefs cf = coefs_of<T, MODE>(a, k.b, k.m);
-  // Thread t takes vectors t, t + 256, t + 512, ... of the chunk, two at a time in
-  // flight: while it forms the directions of one vector, the loads of the next are out,
-  // and each vector's loads are reissued for the vector two steps ahead once it is used.
+  // Thread t takes vectors t, t + 256, t + 512, ... of the chunk with two of them in
+  // flight (buffers A and B): while it forms the directions of one, the next one's loads
+  // are out, and a buffer takes the loads of the vector two steps ahead as soon as its
+  // own vector is done.
   float sg = 0.f, sa = 0.f, sd = 0.f;
   uint4 A[Tr::NIN], B[Tr::NIN];
   int64_t v = k.v_lo + threadIdx.x;
