@@ -27,9 +27,10 @@ constexpr int kNoiseThreads = 128;
 constexpr int kNoiseUnroll = 2;
 constexpr int kNoiseVecPerCta = kNoiseThreads * kNoiseUnroll;
 // Vectors of each input a CTA prefetches into L2 before its dependency wait: with 256
-// vectors a CTA, all of them. (Measured on B300 with 1024-vector CTAs in the stage-3
-// 512x768 step: 256, 384, 512, 640 and 1024 vectors gave 21.24, 21.21, 21.17, 21.15 and
-// 21.30 us per step against 21.35 without.)
+// vectors a CTA, all of them. Measured on B300 in the stage-3 512x768 step: with 256-vector
+// CTAs, 64, 128 and 192 vectors gave 20.66, 20.67 and 20.52 us per step against 20.42 for
+// all 256; with 1024-vector CTAs, 256, 384, 512, 640 and 1024 vectors gave 21.24, 21.21,
+// 21.17, 21.15 and 21.30 us against 21.35 without.
 constexpr int64_t kNoiseEarlyVec = 512;
 
 // The noised samples are read next by the objective: their lines are stored with an
