@@ -55,9 +55,13 @@ struct Traits {
   static constexpr int NG = (kScm ? 4 : 0) + (kDmd ? 2 : 0) + (kCfg ? 1 : 0);
   static constexpr int kYT0 = kScm ? 4 : 0;  // position of y_T among the gradient inputs
   // resident gradient-pass CTAs per SM: three, as for the first pass, so one balanced
-  // wave of chunks is one wave of both kernels (for the seven inputs of the guided
-  // stage-3 pass this spills 80 bytes, and is still 7-8% faster than two per SM)
+  // wave of chunks is one wave of both kernels
   static constexpr int kGradCtas = 3;
+  // vectors per thread in flight in the gradient pass: two, except for the seven inputs
+  // of the guided stage-3 pass, which spilled 96 bytes at two within 80 registers; with
+  // one it needs 72 and ran 18.0 instead of 18.8 us per 512x768 call on B300 (the other
+  // modes lost 0.6 to 1.2 us with one)
+  static constexpr int kGradPer = kCfg ? 1 : kPerThread;
 };
 
 // The teacher prediction at the re-noised sample: the stored one, or with guidance
@@ -472,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, Traits<T, MODE>::kGradCtas)
     k_grads(const __grid_constant__ ObjectiveArgs a) {
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
+  constexpr int kGradBatch = kThreads * Tr::kGradPer;
   __shared__ float3 scratch[kWarps];
   const Chunk k = chunk_of<VE>(a, blockIdx.x);
   const Coefs cf = coefs_of<T, MODE>(a, k.b, k.m);
@@ -479,10 +484,10 @@ __global__ void __launch_bounds__(kThreads, Traits<T, MODE>::kGradCtas)
   const float qnan = __int_as_float(0x7fc00000);
 
   // the first batch's loads (served by L2) are in flight while the totals are read
-  uint4 in[kPerThread][Tr::NG];
+  uint4 in[Tr::kGradPer][Tr::NG];
   int64_t base = k.v_lo;
 #pragma unroll
-  for (int u = 0; u < kPerThread; ++u) {
+  for (int u = 0; u < Tr::kGradPer; ++u) {
     const int64_t v = base + u * kThreads + threadIdx.x;
     if (v < k.v_hi) load_grad_vec<T, MODE>(in[u], a, k.m, k.e_vec0 + v * VE, drop);
   }
@@ -500,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, Traits<T, MODE>::kGradCtas)
 
   for (;;) {
 #pragma unroll
-    for (int u = 0; u < kPerThread; ++u) {
+    for (int u = 0; u < Tr::kGradPer; ++u) {
       const int64_t v = base + u * kThreads + threadIdx.x;
       if (v < k.v_hi) {
         float gs[VE], gd[VE];
@@ -508,10 +513,10 @@ __global__ void __launch_bounds__(kThreads, Traits<T, MODE>::kGradCtas)
         write_vec<T, MODE>(a, k.m, k.e_vec0 + v * VE, scS, scD, gs, gd);
       }
     }
-    base += kBatchVec;
+    base += kGradBatch;
     if (base >= k.v_hi) break;
 #pragma unroll
-    for (int u = 0; u < kPerThread; ++u) {
+    for (int u = 0; u < Tr::kGradPer; ++u) {
       const int64_t v = base + u * kThreads + threadIdx.x;
       if (v < k.v_hi) load_grad_vec<T, MODE>(in[u], a, k.m, k.e_vec0 + v * VE, drop);
     }
