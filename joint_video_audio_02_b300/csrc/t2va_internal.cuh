@@ -104,6 +104,7 @@ struct ObjectiveLaunch {
   int grid;
   int threads;
   size_t smem;
+  int grad_per;  // vectors per thread in flight in the gradient pass: 1 or 2
 };
 // Chooses the chunks and the grid for `a` (fills the plan fields); returns false if
 // the problem is too large for the workspace layout.

@@ -57,11 +57,10 @@ struct Traits {
   // resident gradient-pass CTAs per SM: three, as for the first pass, so one balanced
   // wave of chunks is one wave of both kernels
   static constexpr int kGradCtas = 3;
-  // vectors per thread in flight in the gradient pass: two, except for the seven inputs
-  // of the guided stage-3 pass, which spilled 96 bytes at two within 80 registers; with
-  // one it needs 72 and ran 18.0 instead of 18.8 us per 512x768 call on B300 (the other
-  // modes lost 0.6 to 1.2 us with one)
-  static constexpr int kGradPer = kCfg ? 1 : kPerThread;
+  // the guided stage-3 gradient pass keeps one vector per thread in flight: its seven
+  // inputs spilled 96 bytes at two within 80 registers; with one it needs 72 and ran 18.0
+  // instead of 18.8 us per 512x768 call on B300
+  static constexpr bool kGradOneOnly = kCfg;
 };
 
 // The teacher prediction at the re-noised sample: the stored one, or with guidance
@@ -471,12 +470,13 @@ __device__ __forceinline__ float3 row_totals(const ObjectiveArgs& a, int b, int 
   return block_sum3(x, y, z, scratch);
 }
 
-template <typename T, int MODE>
+// PER: vectors per thread in flight (the plan's choice; see plan_objective).
+template <typename T, int MODE, int PER>
 __global__ void __launch_bounds__(kThreads, Traits<T, MODE>::kGradCtas)
     k_grads(const __grid_constant__ ObjectiveArgs a) {
   using Tr = Traits<T, MODE>;
   constexpr int VE = Tr::VE;
-  constexpr int kGradBatch = kThreads * Tr::kGradPer;
+  constexpr int kGradBatch = kThreads * PER;
   __shared__ float3 scratch[kWarps];
   const Chunk k = chunk_of<VE>(a, blockIdx.x);
   const Coefs cf = coefs_of<T, MODE>(a, k.b, k.m);
@@ -484,10 +484,10 @@ __global__ void __launch_bounds__(kThreads, Traits<T, MODE>::kGradCtas)
   const float qnan = __int_as_float(0x7fc00000);
 
   // the first batch's loads (served by L2) are in flight while the totals are read
-  uint4 in[Tr::kGradPer][Tr::NG];
+  uint4 in[PER][Tr::NG];
   int64_t base = k.v_lo;
 #pragma unroll
-  for (int u = 0; u < Tr::kGradPer; ++u) {
+  for (int u = 0; u < PER; ++u) {
     const int64_t v = base + u * kThreads + threadIdx.x;
     if (v < k.v_hi) load_grad_vec<T, MODE>(in[u], a, k.m, k.e_vec0 + v * VE, drop);
   }
@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, Traits<T, MODE>::kGradCtas)
 
   for (;;) {
 #pragma unroll
-    for (int u = 0; u < Tr::kGradPer; ++u) {
+    for (int u = 0; u < PER; ++u) {
       const int64_t v = base + u * kThreads + threadIdx.x;
       if (v < k.v_hi) {
         float gs[VE], gd[VE];
@@ -516,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, Traits<T, MODE>::kGradCtas)
     base += kGradBatch;
     if (base >= k.v_hi) break;
 #pragma unroll
-    for (int u = 0; u < Tr::kGradPer; ++u) {
+    for (int u = 0; u < PER; ++u) {
       const int64_t v = base + u * kThreads + threadIdx.x;
       if (v < k.v_hi) load_grad_vec<T, MODE>(in[u], a, k.m, k.e_vec0 + v * VE, drop);
     }
@@ -592,7 +592,12 @@ template <typename T, int MODE>
 cudaError_t launch_t(const ObjectiveArgs& a, const ObjectiveLaunch& l, cudaStream_t st) {
   cudaError_t e = launch_pdl(k_sums<T, MODE>, l.grid, st, a);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_grads<T, MODE>, l.grid, st, a);
+  if constexpr (Traits<T, MODE>::kGradOneOnly) {
+    return launch_pdl(k_grads<T, MODE, 1>, l.grid, st, a);
+  } else {
+    if (l.grad_per == 1) return launch_pdl(k_grads<T, MODE, 1>, l.grid, st, a);
+    return launch_pdl(k_grads<T, MODE, 2>, l.grid, st, a);
+  }
 }
 
 __global__ void k_ws_init(uint4* ws, size_t n16) {
@@ -671,6 +676,13 @@ bool plan_objective(ObjectiveArgs& a, t2va_dtype dt, int sm_count, ObjectiveLaun
   out->grid = (int)grid;
   out->threads = kThreads;
   out->smem = 0;
+  // Two vectors per thread in flight in the gradient pass when the call is one wave of
+  // chunks longer than a vector per thread; one otherwise: with inputs beyond L2 the pass
+  // re-reads them from HBM, and at one vector a thread needs about 63 registers, so four
+  // CTAs fit on an SM where the later waves run. Measured on B300 (per call): 512x768
+  // batch 4 15.9 us with two against 16.8 with one, 1024x1792 18.9 against 19.5; the
+  // batch-16 sweep shape (multi-wave) 70.5 with one against 71.7, batch 1 7.40 against 7.56.
+  out->grad_per = (grid <= wave && a.vpc > kThreads) ? 2 : 1;
   return true;
 }
 
