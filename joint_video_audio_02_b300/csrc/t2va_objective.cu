@@ -38,10 +38,12 @@ constexpr int kPerThread = 2;                    // vectors per thread per batch
 constexpr int kBatchVec = kThreads * kPerThread;  // vectors per CTA per batch
 constexpr int64_t kMaxWaveVec = 2048;             // longest chunk of a one-wave plan
 // Vectors at the start of a chunk that k_sums prefetches into L2 before its dependency
-// wait. Measured on B300 with caps of 192 to 384 vectors and with 1/8 to all of the
-// chunk: 256 to 320 is best at every stage-3 shape tried; prefetching more, or one batch
-// ahead inside the loop as well, loses.
+// wait, per input. Measured on B300 with caps of 192 to 384 vectors and with 1/8 to all of
+// the chunk: 256 to 320 is best at every stage-3 shape tried; prefetching more, or one
+// batch ahead inside the loop as well, loses. The sCM objective alone (four inputs) is
+// best at 384: 10.76 against 10.90 us per 512x768 call with 320.
 constexpr int64_t kEarlyVec = 320;
+constexpr int64_t kEarlyVecScmOnly = 384;
 
 template <typename T, int MODE>
 struct Traits {
@@ -397,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_sums(const __grid_constant__ Ob
   // The HBM stream starts while the previous kernel drains: thread q asks L2 for the
   // chunk's first kEarlyVec vectors of input q. (Only a prefetch may run this early.)
   if (threadIdx.x < Tr::NIN && k.v_hi > k.v_lo) {
-    const int64_t nv = min(k.v_hi - k.v_lo, kEarlyVec);
+    const int64_t nv = min(k.v_hi - k.v_lo, Tr::kDmd ? kEarlyVec : kEarlyVecScmOnly);
     prefetch_l2(reinterpret_cast<const T*>(a.in[Tr::k0 + threadIdx.x][k.m]) + k.e_vec0 + k.v_lo * VE,
                 (uint32_t)(nv * 16), keep);
   }
